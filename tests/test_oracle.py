@@ -1,0 +1,288 @@
+"""Pins for the CPU oracle: it is checked against closed forms, hand-written examples, library routines, brute force
+and invariants of the mathematics, never against itself. CPU only."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ------------------------------------------------------------------------------------------ dtype rounding
+
+
+def test_round_to_bf16_ties_to_even():
+    # 1 + 2^-8 is halfway between bf16 neighbours 1 and 1 + 2^-7: ties go to the even mantissa (1.0);
+    # 1 + 3*2^-8 is halfway between 1 + 2^-7 and 1 + 2^-6: goes to 1 + 2^-6.
+    x = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, 1 + 2 ** -8 + 2 ** -20, -(1 + 2 ** -8)], np.float32)
+    assert O.round_to(x, "bf16").tolist() == [1.0, 1 + 2 ** -6, 1 + 2 ** -7, -1.0]
+
+
+def test_round_to_fp16_ties_to_even():
+    # fp16 has 10 fraction bits: 1 + 2^-11 is a tie -> 1.0; 1 + 3*2^-11 -> 1 + 2^-9
+    x = np.array([1 + 2 ** -11, 1 + 3 * 2 ** -11, 2049.0, 2051.0], np.float32)
+    assert O.round_to(x, "fp16").tolist() == [1.0, 1 + 2 ** -9, 2048.0, 2052.0]
+
+
+def test_bits16_roundtrip_and_known_patterns():
+    assert O.bits16(np.array([1.0, -2.0], np.float32), "bf16").tolist() == [0x3F80, 0xC000]
+    assert O.bits16(np.array([1.0, -2.0], np.float32), "fp16").tolist() == [0x3C00, 0xC000]
+    v = O.round_to(np.random.default_rng(0).standard_normal(1000).astype(np.float32), "bf16")
+    assert np.array_equal(O.from_bits16(O.bits16(v, "bf16"), "bf16"), v)
+
+
+# ------------------------------------------------------------------------------------------ pack / unpack
+
+
+def _golden_pack():
+    rows = []
+    with open(os.path.join(GOLDEN, "pack_examples.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            bits, codes, word = (p.strip() for p in line.split("|"))
+            rows.append((int(bits), [int(c) for c in codes.split()], int(word, 16)))
+    return rows
+
+
+@pytest.mark.parametrize("bits,codes,word", _golden_pack())
+def test_pack_golden(bits, codes, word):
+    w = O.pack(np.array(codes, np.uint32), bits)
+    assert w.tolist() == [word]
+    assert O.unpack(np.array([word], np.uint32), bits, len(codes)).tolist() == codes
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_pack_roundtrip_random_words(bits):
+    # random words -> codes -> words must be the identity (bit-exact) over 1e6 words
+    rng = np.random.default_rng(bits)
+    per = 32 // bits
+    words = rng.integers(0, 2 ** 32, size=(1000, 1000), dtype=np.uint64).astype(np.uint32)
+    codes = O.unpack(words, bits, 1000 * per)
+    assert codes.max() < 2 ** bits
+    assert np.array_equal(O.pack(codes, bits), words)
+
+
+def test_pack_bit_positions_one_hot():
+    # every single code position lands on its own bit field
+    for bits in (4, 8):
+        per = 32 // bits
+        for i in range(per):
+            c = np.zeros(per, np.uint32)
+            c[i] = 1
+            assert O.pack(c, bits)[0] == 1 << (bits * i)
+
+
+# ------------------------------------------------------------------------------------------ quantizer
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("GS", [32, 64, 128])
+def test_quantize_closed_form_4bit(dtype, GS):
+    # a group holding integers with min -1 and max 14: scale (14 - -1)/15 = 1 and bias -1 exactly,
+    # every code is x + 1, the min maps to 0 and the max to 15
+    rng = np.random.default_rng(GS)
+    x = rng.integers(-1, 15, size=(3, GS)).astype(np.float32)
+    x[:, 0], x[:, 1] = -1, 14
+    c, s, b = O.quantize(x, GS, 4, dtype)
+    assert s.tolist() == [[1.0]] * 3 and b.tolist() == [[-1.0]] * 3
+    assert np.array_equal(c, (x + 1).astype(np.uint32))
+    assert np.array_equal(O.dequantize(c, s, b, GS), x.astype(np.float64))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_quantize_closed_form_8bit(dtype):
+    # integers 0..255 with scale 255/255 = 1 and bias 0: codes are the values themselves
+    x = np.arange(256, dtype=np.float32).reshape(8, 32)[::-1].copy()
+    x[:, 0], x[:, 1] = 0, 255
+    c, s, b = O.quantize(x, 32, 8, dtype)
+    assert np.all(s == 1.0) and np.all(b == 0.0)
+    assert np.array_equal(c, x.astype(np.uint32))
+
+
+def test_quantize_scale_is_range_over_levels():
+    # a two-value group {0, 3}: 4-bit scale 3/15 = 0.2 (rounded to bf16), 8-bit 3/255
+    x = np.zeros((1, 32), np.float32)
+    x[0, 5] = 3.0
+    _, s4, b4 = O.quantize(x, 32, 4, "bf16")
+    _, s8, _ = O.quantize(x, 32, 8, "fp16")
+    assert s4[0, 0] == torch.tensor(0.2).to(torch.bfloat16).float().item()
+    assert s8[0, 0] == torch.tensor(3.0 / 255.0).to(torch.float16).float().item()
+    assert b4[0, 0] == 0.0
+
+
+def test_quantize_zero_range_group():
+    x = np.full((2, 64), 0.3, np.float32)
+    c, s, b = O.quantize(x, 64, 4, "bf16")
+    assert np.all(c == 0) and np.all(s == 0)
+    assert np.all(b == np.float32(torch.tensor(0.3).to(torch.bfloat16).float().item()))
+
+
+def test_quantize_rounds_half_to_even():
+    # scale 1, bias 0; values 0.5, 1.5, 2.5 sit on ties -> codes 0, 2, 2
+    x = np.zeros((1, 32), np.float32)
+    x[0, :4] = [0.0, 0.5, 1.5, 2.5]
+    x[0, 4] = 15.0
+    c, s, b = O.quantize(x, 32, 4, "bf16")
+    assert s[0, 0] == 1.0 and b[0, 0] == 0.0
+    assert c[0, :4].tolist() == [0, 0, 2, 2]
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_quantize_error_bound(bits, dtype):
+    # |x - x_hat| <= s_hat/2 plus what rounding the scale and bias to 16 bits can add at the clamped ends,
+    # and the bound is nearly reached (a floor instead of a round would break the first, a coarser grid the second)
+    rng = np.random.default_rng(3)
+    GS = 64
+    x = rng.standard_normal((512, 4 * GS)).astype(np.float32)
+    c, s, b = O.quantize(x, GS, bits, dtype)
+    xh = O.dequantize(c, s, b, GS).reshape(512, 4, GS)
+    g = x.reshape(512, 4, GS).astype(np.float64)
+    lo, hi = g.min(-1), g.max(-1)
+    qmax = 2 ** bits - 1
+    exact_scale = (hi - lo) / qmax
+    slack = qmax * np.abs(s - exact_scale) + np.abs(b - lo) + 1e-6 * np.abs(g).max(-1)
+    err = np.abs(xh - g).max(-1)
+    assert np.all(err <= s / 2 + slack)
+    assert np.median(err / s) > 0.4
+
+
+# ------------------------------------------------------------------------------------------ attention
+
+
+def _softmax_loop(q, K, V):
+    # brute force with Python floats and math.exp: an independent restatement of softmax(q.K^T/sqrt(D)).V
+    D = len(q)
+    s = [sum(q[d] * K[n][d] for d in range(D)) / math.sqrt(D) for n in range(len(K))]
+    m = max(s)
+    e = [math.exp(v - m) for v in s]
+    z = sum(e)
+    return [sum(e[n] * V[n][d] for n in range(len(K))) / z for d in range(D)]
+
+
+@pytest.mark.parametrize("D", [32, 64])
+@pytest.mark.parametrize("N", [1, 2, 5, 8])
+def test_attention_brute_force_tiny(D, N):
+    rng = np.random.default_rng(N * 100 + D)
+    H, Hkv, GS, bits = 4, 2, 32, 4
+    q = O.round_to(rng.standard_normal((H, D)).astype(np.float32), "bf16").astype(np.float64)
+    Kx = rng.standard_normal((Hkv, N, D)).astype(np.float32)
+    Vx = rng.standard_normal((Hkv, N, D)).astype(np.float32)
+    kc, ks, kb = O.quantize(Kx, GS, bits, "bf16")
+    vc, vs, vb = O.quantize(Vx, GS, bits, "bf16")
+    K = O.dequantize(kc, ks, kb, GS)
+    V = O.dequantize(vc, vs, vb, GS)
+    out = O.attention(q, K, V)
+    # library routine: scaled_dot_product_attention in fp64 on the dequantized arrays (its default scale is
+    # 1/sqrt(D)); GQA by repeating each KV head over its group of query heads
+    nrep = H // Hkv
+    Kr = torch.from_numpy(np.repeat(K, nrep, axis=0))[:, None]
+    Vr = torch.from_numpy(np.repeat(V, nrep, axis=0))[:, None]
+    ref = torch.nn.functional.scaled_dot_product_attention(torch.from_numpy(q)[:, None, None], Kr, Vr)
+    np.testing.assert_allclose(out, ref[:, 0, 0].numpy(), rtol=1e-12, atol=1e-12)
+    for h in range(H):
+        loop = _softmax_loop(q[h].tolist(), K[h // nrep].tolist(), V[h // nrep].tolist())
+        np.testing.assert_allclose(out[h], loop, rtol=1e-11, atol=1e-12)
+
+
+def test_attention_scale_closed_form():
+    # two keys, k0 = 0 and k1 = c*e_0; with q = e_0 the weights are 1 : e^(c/sqrt(D))
+    D, c = 64, 3.0
+    q = np.zeros(D)
+    q[0] = 1.0
+    K = np.zeros((2, D))
+    K[1, 0] = c
+    V = np.zeros((2, D))
+    V[0, 1], V[1, 1] = 1.0, 0.0
+    w = math.exp(c / math.sqrt(D))
+    out = O.attention_head(q, K, V)
+    assert abs(out[1] - 1.0 / (1.0 + w)) < 1e-15
+
+
+def test_attention_all_equal_scores_is_mean_of_v():
+    rng = np.random.default_rng(11)
+    N, D = 97, 64
+    row = rng.standard_normal(D)
+    K = np.tile(row, (N, 1))
+    V = rng.standard_normal((N, D))
+    q = rng.standard_normal(D)
+    np.testing.assert_allclose(O.attention_head(q, K, V), V.mean(0), rtol=1e-12, atol=1e-13)
+
+
+def test_attention_one_hot_dominant_key():
+    rng = np.random.default_rng(12)
+    N, D = 64, 64
+    q = np.zeros(D)
+    q[3] = 1.0
+    K = rng.standard_normal((N, D)) * 0.01
+    j = 17
+    K[j, 3] = 60.0 * math.sqrt(D) + 1.0          # score margin >= 60 over every other key
+    V = rng.uniform(-1, 1, (N, D))
+    out = O.attention_head(q, K, V)
+    assert np.abs(out - V[j]).max() < N * math.exp(-60) * 2
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 7, 40])
+def test_blocked_equals_unblocked(S):
+    rng = np.random.default_rng(S)
+    N, D = 40, 64
+    q = rng.standard_normal(D) * 3
+    K = rng.standard_normal((N, D))
+    V = rng.standard_normal((N, D))
+    ref = O.attention_head(q, K, V)
+    blk = O.attention_blocked(q, K, V, S)
+    assert np.abs(blk - ref).max() <= 1e-12 * np.abs(ref).max()
+
+
+def test_factored_dot_identity():
+    # sum_d (s*c_d + b) q_d == s * sum_d c_d q_d + b * sum_d q_d per group (the dequant factored out of the dot)
+    rng = np.random.default_rng(5)
+    D, GS = 256, 64
+    x = rng.standard_normal((16, D)).astype(np.float32)
+    c, s, b = O.quantize(x, GS, 4, "bf16")
+    q = rng.standard_normal(D)
+    direct = O.dequantize(c, s, b, GS) @ q
+    cg = c.reshape(16, D // GS, GS).astype(np.float64)
+    qg = q.reshape(D // GS, GS)
+    factored = (s * (cg * qg).sum(-1) + b * qg.sum(-1)).sum(-1)
+    np.testing.assert_allclose(direct, factored, rtol=1e-12, atol=1e-12)
+
+
+def test_gqa_head_map_is_contiguous():
+    # kv head j serves query heads j*nrep .. j*nrep + nrep - 1 (not h % Hkv)
+    H, Hkv, N, D = 8, 2, 5, 32
+    q = np.random.default_rng(0).standard_normal((H, D))
+    K = np.zeros((Hkv, N, D))
+    V = np.stack([np.full((N, D), 1.0), np.full((N, D), 2.0)])
+    out = O.attention(q, K, V)
+    assert np.all(out[:4] == 1.0) and np.all(out[4:] == 2.0)
+
+
+def test_packed_interface_ragged_layout():
+    # sequences back to back, [Hkv, N[b], .] each: the packed path must agree with per-sequence dequantized math
+    rng = np.random.default_rng(9)
+    N = [3, 7, 1]
+    B, H, Hkv, D, GS, bits = 3, 4, 2, 64, 32, 8
+    rows = Hkv * sum(N)
+    Kx = rng.standard_normal((rows, D)).astype(np.float32)
+    Vx = rng.standard_normal((rows, D)).astype(np.float32)
+    kp, ks, kb, vp, vs, vb = O.quantize_cache(Kx, Vx, GS, bits, "fp16")
+    q = rng.standard_normal((B, H, D))
+    got = O.attention_packed(q, kp, ks, kb, vp, vs, vb, N, H, Hkv, D, GS, bits)
+    r = 0
+    for b, n in enumerate(N):
+        Kb = np.stack([O.dequantize(*O.quantize(Kx[r + j * n: r + (j + 1) * n], GS, bits, "fp16"), GS)
+                       for j in range(Hkv)])
+        Vb = np.stack([O.dequantize(*O.quantize(Vx[r + j * n: r + (j + 1) * n], GS, bits, "fp16"), GS)
+                       for j in range(Hkv)])
+        ref = O.attention(q[b], Kb, Vb)
+        for h in range(H):
+            np.testing.assert_array_equal(got[(b, h)], ref[h])
+        r += Hkv * n
+    assert r == rows
