@@ -1,0 +1,152 @@
+"""Quantized-KV single-query decode attention for GB300 (sm_103a).
+
+The work happens in libqdecode_attn.so (hand-written CUDA behind a C ABI, include/qdecode_attn.h). This module
+only marshals torch tensors (device memory and streams) into that ABI, under the same names.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import (QDA_BF16, QDA_FP16, QDA_FP32, QdaError, QdaPlan, lib)  # noqa: F401
+
+_DT_CODE = {torch.bfloat16: QDA_BF16, torch.float16: QDA_FP16, torch.float32: QDA_FP32}
+_CODE_DT = {v: k for k, v in _DT_CODE.items()}
+
+
+def dtype_code(in_dtype: torch.dtype, out_dtype: Optional[torch.dtype] = None) -> int:
+    """The ABI's dtype argument: input dtype in the low byte, output dtype in the next."""
+    return _DT_CODE[in_dtype] | ((_DT_CODE[out_dtype] if out_dtype is not None else 0) << 8)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def qdecode_attn(q: torch.Tensor, k_packed: torch.Tensor, k_scales: torch.Tensor, k_biases: torch.Tensor,
+                 v_packed: torch.Tensor, v_scales: torch.Tensor, v_biases: torch.Tensor, out: torch.Tensor,
+                 N: Sequence[int], Hkv: int, GS: int, bits: int, stream=None) -> torch.Tensor:
+    """out[b, h] = softmax(q[b, h] . K_hat[b, h // (H/Hkv)]^T / sqrt(D)) V_hat[...] from the packed cache.
+
+    q ``[B, H, D]`` bf16/fp16; packed ``[Hkv * sum(N), D*bits/32]`` int32/uint32 (sequences back to back, each
+    ``[Hkv, N[b], .]``); scales/biases ``[Hkv * sum(N), D/GS]`` in q's dtype; out ``[B, H, D]`` (bf16, fp16 or
+    fp32). Asynchronous on ``stream`` (default: torch's current stream).
+    """
+    B, H, D = q.shape
+    n = _lib.int32_array(N)
+    st = lib().qdecode_attn(_ptr(q), _ptr(k_packed), _ptr(k_scales), _ptr(k_biases), _ptr(v_packed),
+                            _ptr(v_scales), _ptr(v_biases), _ptr(out), B, H, Hkv, n, D, GS, bits,
+                            dtype_code(q.dtype, out.dtype), _stream(stream))
+    _lib.check(st, "qdecode_attn")
+    return out
+
+
+def qdecode_attn_plan(B: int, H: int, Hkv: int, N: Sequence[int], D: int, GS: int, bits: int, num_sms: int = 0,
+                      ctas_per_sm: int = 0) -> dict:
+    plan = QdaPlan()
+    st = lib().qdecode_attn_plan(B, H, Hkv, _lib.int32_array(N), D, GS, bits, num_sms, ctas_per_sm,
+                                 ctypes.byref(plan))
+    _lib.check(st, "qdecode_attn_plan")
+    return plan.as_dict()
+
+
+def qdecode_attn_workspace_bytes(B: int, H: int, Hkv: int, N: Sequence[int], D: int, GS: int, bits: int) -> int:
+    out = ctypes.c_size_t()
+    st = lib().qdecode_attn_workspace_bytes(B, H, Hkv, _lib.int32_array(N), D, GS, bits, ctypes.byref(out))
+    _lib.check(st, "qdecode_attn_workspace_bytes")
+    return out.value
+
+
+def qdecode_attn_set_workspace(buf: Optional[torch.Tensor]) -> None:
+    st = lib().qdecode_attn_set_workspace(_ptr(buf), 0 if buf is None else buf.numel() * buf.element_size())
+    _lib.check(st, "qdecode_attn_set_workspace")
+
+
+def qdecode_attn_debug_force_splits(num_ctas: int) -> None:
+    _lib.check(lib().qdecode_attn_debug_force_splits(num_ctas), "qdecode_attn_debug_force_splits")
+
+
+def qdecode_attn_set_split_event(event: Optional[torch.cuda.Event]) -> None:
+    handle = None if event is None else event.cuda_event
+    _lib.check(lib().qdecode_attn_set_split_event(handle), "qdecode_attn_set_split_event")
+
+
+def qdecode_quantize(x: torch.Tensor, GS: int, bits: int, dtype: torch.dtype, packed: torch.Tensor,
+                     scales: torch.Tensor, biases: torch.Tensor, stream=None) -> None:
+    """Quantize fp32 rows ``x [rows, D]`` into ``packed [rows, D*bits/32]``, ``scales``/``biases [rows, D/GS]``
+    (dtype bf16 or fp16). Writing into views offset to a cache's next rows appends to that cache."""
+    rows, D = x.shape
+    st = lib().qdecode_quantize(_ptr(x), rows, D, GS, bits, dtype_code(dtype), _ptr(packed), _ptr(scales),
+                                _ptr(biases), _stream(stream))
+    _lib.check(st, "qdecode_quantize")
+
+
+def qdecode_attn_device_status() -> int:
+    flags = ctypes.c_uint()
+    _lib.check(lib().qdecode_attn_device_status(ctypes.byref(flags)), "qdecode_attn_device_status")
+    return flags.value
+
+
+def qdecode_attn_calls() -> int:
+    return lib().qdecode_attn_calls()
+
+
+# ------------------------------------------------------------------------------------------- conveniences
+
+
+class QuantizedKV:
+    """A packed cache in the library's layout: sequences back to back, each ``[Hkv, N[b], .]``."""
+
+    def __init__(self, packed_k, scales_k, biases_k, packed_v, scales_v, biases_v, N, Hkv, D, GS, bits):
+        self.kp, self.ks, self.kb = packed_k, scales_k, biases_k
+        self.vp, self.vs, self.vb = packed_v, scales_v, biases_v
+        self.N, self.Hkv, self.D, self.GS, self.bits = list(N), Hkv, D, GS, bits
+
+    @classmethod
+    def empty(cls, N, Hkv, D, GS, bits, dtype, device="cuda"):
+        rows = Hkv * sum(N)
+        W, NG = D * bits // 32, D // GS
+        mk = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)  # noqa: E731
+        return cls(mk((rows, W), torch.int32), mk((rows, NG), dtype), mk((rows, NG), dtype),
+                   mk((rows, W), torch.int32), mk((rows, NG), dtype), mk((rows, NG), dtype), N, Hkv, D, GS, bits)
+
+    @property
+    def dtype(self):
+        return self.ks.dtype
+
+    def unit_rows(self, b: int, kvh: int):
+        r0 = self.Hkv * sum(self.N[:b]) + kvh * self.N[b]
+        return r0, r0 + self.N[b]
+
+    def quantize_into(self, b: int, kvh: int, K: torch.Tensor, V: torch.Tensor, row0: int = 0, stream=None):
+        """Quantize fp32 K, V rows ``[n, D]`` into rows ``row0 .. row0 + n`` of KV head ``kvh`` of sequence b."""
+        r0, r1 = self.unit_rows(b, kvh)
+        a = r0 + row0
+        e = a + K.shape[0]
+        if e > r1:
+            raise ValueError("rows past the end of this KV head")
+        qdecode_quantize(K, self.GS, self.bits, self.dtype, self.kp[a:e], self.ks[a:e], self.kb[a:e], stream)
+        qdecode_quantize(V, self.GS, self.bits, self.dtype, self.vp[a:e], self.vs[a:e], self.vb[a:e], stream)
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.kp, self.ks, self.kb, self.vp, self.vs, self.vb))
+
+
+def decode_attention(q: torch.Tensor, cache: QuantizedKV, out_dtype: Optional[torch.dtype] = None,
+                     out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Allocating wrapper of qdecode_attn over a QuantizedKV."""
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
+    return qdecode_attn(q, cache.kp, cache.ks, cache.kb, cache.vp, cache.vs, cache.vb, out, cache.N, cache.Hkv,
+                        cache.GS, cache.bits, stream)

@@ -1,0 +1,84 @@
+// Internal definitions shared by the host entry points and the sm_103a kernels of libqdecode_attn.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "qdecode_attn.h"
+
+#define QDA_NW 4                         // consumer warps per CTA of the split kernel
+#define QDA_THREADS ((QDA_NW + 1) * 32)  // + one producer warp that drives the bulk copies
+
+// Launch parameters of the split and merge kernels (passed by value as a __grid_constant__).
+struct QdaParams {
+  const void* q;              // [B, H, D] input dtype
+  const uint32_t* kp;         // packed K codes, rows of W words
+  const uint16_t* ks;         // K scales, rows of NG 16-bit values
+  const uint16_t* kb;         // K biases
+  const uint32_t* vp;
+  const uint16_t* vs;
+  const uint16_t* vb;
+  float* part_o;              // [slots, heads_pad, D] unnormalised partial outputs
+  float2* part_ml;            // [slots, heads_pad] (running max in log2 units, sum of 2^(s - max))
+  unsigned int* err;          // device error word
+  long long total_rows;       // T = Hkv * sum(N)
+  int B, H, Hkv, D, GS, NG, W, nrep, heads_pad, num_ctas, tile_rows, stages;
+  float qscale;               // log2(e) / sqrt(D): scores come out in log2 units
+  int seq_off[QDA_MAX_B + 1]; // seq_off[b] = N[0] + ... + N[b-1]
+};
+
+// Row range of CTA c: [qda_cta_row(c), qda_cta_row(c + 1)). Interior boundaries are multiples of 8 rows so that
+// every scale/bias tile a CTA copies starts on a 16-byte boundary whatever the group count per row.
+__host__ __device__ inline long long qda_cta_row(long long T, int C, int c) {
+  if (c >= C) return T;
+  if (c <= 0) return 0;
+  return ((T * (long long)c) / C) & ~7LL;
+}
+
+// CTA whose row range holds row r (empty ranges are skipped).
+__host__ __device__ inline int qda_cta_of(long long T, int C, long long r) {
+  int c = (int)((r * (long long)C) / T);
+  if (c >= C) c = C - 1;
+  while (c + 1 < C && qda_cta_row(T, C, c + 1) <= r) ++c;
+  while (c > 0 && qda_cta_row(T, C, c) > r) --c;
+  return c;
+}
+
+// Shared-memory layout of the split kernel.
+struct QdaSmemLayout {
+  size_t codes_bytes;   // one tensor's packed codes for tile_rows rows
+  size_t sc_bytes;      // one scale/bias array for tile_rows rows (multiple of 16)
+  size_t stage_bytes;   // K codes, V codes, K scales, K biases, V scales, V biases
+  size_t stage0;        // offset of stage 0 (after the barriers)
+  size_t comb;          // offset of the cross-warp combine area
+  size_t total;
+};
+
+__host__ __device__ inline QdaSmemLayout qda_smem_layout(int tile_rows, int stages, int W, int NG, int NH, int D) {
+  QdaSmemLayout L;
+  L.codes_bytes = (size_t)tile_rows * W * 4;
+  L.sc_bytes = ((size_t)tile_rows * NG * 2 + 15) & ~(size_t)15;
+  L.stage_bytes = 2 * L.codes_bytes + 4 * L.sc_bytes;
+  L.stage0 = 256;
+  L.comb = L.stage0 + (size_t)stages * L.stage_bytes;
+  L.total = L.comb + (size_t)QDA_NW * NH * D * 4 + (size_t)QDA_NW * NH * 2 * 4;
+  return L;
+}
+
+// Launchers (one translation unit per bits x input dtype). They return cudaSuccess or the launch error.
+// blk: the (bits, words-per-lane, lanes-per-row, heads-per-CTA) variant; grid = (num_ctas, head_chunks).
+cudaError_t qda_launch_split_b4_bf16(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s);
+cudaError_t qda_launch_split_b4_fp16(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s);
+cudaError_t qda_launch_split_b8_bf16(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s);
+cudaError_t qda_launch_split_b8_fp16(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s);
+cudaError_t qda_occupancy_split_b4_bf16(int wpl, int lpr, int nh, size_t smem, int* ctas_per_sm);
+cudaError_t qda_occupancy_split_b4_fp16(int wpl, int lpr, int nh, size_t smem, int* ctas_per_sm);
+cudaError_t qda_occupancy_split_b8_bf16(int wpl, int lpr, int nh, size_t smem, int* ctas_per_sm);
+cudaError_t qda_occupancy_split_b8_fp16(int wpl, int lpr, int nh, size_t smem, int* ctas_per_sm);
+
+cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool pdl, cudaStream_t s);
+
+cudaError_t qda_launch_quantize(const float* x, long long rows, int D, int GS, int bits, int in_dtype,
+                                uint32_t* packed, uint16_t* scales, uint16_t* biases, cudaStream_t s);

@@ -1,0 +1,234 @@
+// Merge kernel (fixed-order combine of the split partials) and the cache quantizer, sm_103a.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "qda_internal.h"
+#include "qda_ptx.cuh"
+
+namespace qda {
+
+__device__ __forceinline__ float ex2m(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int OUT>
+__device__ __forceinline__ void store4(void* out, size_t idx, float4 v) {
+  if constexpr (OUT == QDA_FP32) {
+    reinterpret_cast<float4*>(out)[idx] = v;
+  } else if constexpr (OUT == QDA_BF16) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    reinterpret_cast<uint2*>(out)[idx] = u;
+  } else {
+    __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    reinterpret_cast<uint2*>(out)[idx] = u;
+  }
+}
+
+// out[b, h, :] = sum_s o_s 2^(m_s - M) / sum_s l_s 2^(m_s - M) over the partial slots of (b, KV head of h)
+// (mlx-bun fused-decode-kernel.ts, MERGE_SOURCE), in log2 units. One CTA per (b, h); the slots are dealt to
+// 256 / (D/4) thread groups round-robin and the groups are summed in a fixed order: deterministic, no atomics.
+template <int OUT>
+__global__ void __launch_bounds__(256) qda_merge_kernel(const __grid_constant__ QdaParams p, void* __restrict__ out) {
+  pdl_wait();
+  const int D = p.D;
+  const int tpr = D >> 2;
+  const int groups = blockDim.x / tpr;
+  const int grp = threadIdx.x / tpr, t = threadIdx.x - grp * tpr;
+  const int bh = blockIdx.x;
+  const int b = bh / p.H, h = bh - b * p.H;
+  const int kvh = h / p.nrep, j = h - kvh * p.nrep;
+  const int unit = b * p.Hkv + kvh;
+  const long long n = p.seq_off[b + 1] - p.seq_off[b];
+  const long long us = (long long)p.Hkv * p.seq_off[b] + (long long)kvh * n;
+  const long long T = p.total_rows;
+  const int cf = qda_cta_of(T, p.num_ctas, us);
+  const int cl = qda_cta_of(T, p.num_ctas, us + n - 1);
+
+  // CTAs with an empty row range (possible only when ranges are shorter than 8 rows) wrote no slot
+  float M = -INFINITY;
+  for (int c = cf; c <= cl; ++c) {
+    if (qda_cta_row(T, p.num_ctas, c) == qda_cta_row(T, p.num_ctas, c + 1)) continue;
+    M = fmaxf(M, p.part_ml[(size_t)(c + unit) * p.heads_pad + j].x);
+  }
+
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  for (int c = cf + grp; c <= cl; c += groups) {
+    if (qda_cta_row(T, p.num_ctas, c) == qda_cta_row(T, p.num_ctas, c + 1)) continue;
+    const size_t hp = (size_t)(c + unit) * p.heads_pad + j;
+    const float2 ml = p.part_ml[hp];
+    const float wt = ex2m(ml.x - M);
+    den = fmaf(ml.y, wt, den);
+    const float4 v = reinterpret_cast<const float4*>(p.part_o + hp * D)[t];
+    acc.x = fmaf(v.x, wt, acc.x);
+    acc.y = fmaf(v.y, wt, acc.y);
+    acc.z = fmaf(v.z, wt, acc.z);
+    acc.w = fmaf(v.w, wt, acc.w);
+  }
+  __shared__ float4 red[256];
+  __shared__ float dred[256];
+  red[threadIdx.x] = acc;
+  if (t == 0) dred[grp] = den;
+  __syncthreads();
+  if (grp != 0) return;
+  float dt = dred[0];
+  for (int g = 1; g < groups; ++g) {
+    const float4 v = red[g * tpr + t];
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+    dt += dred[g];
+  }
+  const float inv = 1.0f / dt;
+  acc.x *= inv;
+  acc.y *= inv;
+  acc.z *= inv;
+  acc.w *= inv;
+  store4<OUT>(out, ((size_t)bh * D >> 2) + t, acc);
+}
+
+// ------------------------------------------------------------------------------------------- quantizer
+
+template <bool F16>
+__device__ __forceinline__ uint32_t round_bits16(float x) {
+  if constexpr (F16) {
+    return __half_as_ushort(__float2half_rn(x));
+  } else {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  }
+}
+
+// One warp per row of D = 32 * E fp32 values; lane l holds elements [l*E, l*E + E). A group spans GS/E lanes.
+template <int BITS, int E, bool F16>
+__global__ void __launch_bounds__(256) qda_quant_kernel(const float* __restrict__ x, long long rows, int GS,
+                                                        uint32_t* __restrict__ packed, uint16_t* __restrict__ sc,
+                                                        uint16_t* __restrict__ bi) {
+  constexpr int D = 32 * E;
+  constexpr int PER = 32 / BITS;
+  constexpr int W = D / PER;
+  constexpr float QMAX = (float)((1 << BITS) - 1);
+  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const float* xr = x + row * D + lane * E;
+  float v[E];
+  if constexpr (E % 4 == 0) {
+#pragma unroll
+    for (int k = 0; k < E / 4; ++k) {
+      const float4 t = reinterpret_cast<const float4*>(xr)[k];
+      v[4 * k] = t.x;
+      v[4 * k + 1] = t.y;
+      v[4 * k + 2] = t.z;
+      v[4 * k + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < E / 2; ++k) {
+      const float2 t = reinterpret_cast<const float2*>(xr)[k];
+      v[2 * k] = t.x;
+      v[2 * k + 1] = t.y;
+    }
+  }
+  float lo = v[0], hi = v[0];
+#pragma unroll
+  for (int e = 1; e < E; ++e) {
+    lo = fminf(lo, v[e]);
+    hi = fmaxf(hi, v[e]);
+  }
+  const int lpg = GS / E;
+  for (int off = 1; off < lpg; off <<= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+  }
+  const float scale = __fdiv_rn(__fsub_rn(hi, lo), QMAX);
+  const uint32_t sbits = round_bits16<F16>(scale);
+  const uint32_t bbits = round_bits16<F16>(lo);
+  const float s_hat = half_bits_to_float<F16>(sbits);
+  const float b_hat = half_bits_to_float<F16>(bbits);
+  uint32_t code[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    float r = rintf(__fdiv_rn(__fsub_rn(v[e], b_hat), s_hat));
+    r = fminf(fmaxf(r, 0.f), QMAX);
+    code[e] = (s_hat == 0.f) ? 0u : (uint32_t)r;
+  }
+  if constexpr (E * BITS >= 32) {
+    constexpr int WL = E * BITS / 32;  // whole words per lane
+#pragma unroll
+    for (int w = 0; w < WL; ++w) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int k = 0; k < PER; ++k) word |= code[w * PER + k] << (BITS * k);
+      packed[row * W + lane * WL + w] = word;
+    }
+  } else {
+    constexpr int LPW = 32 / (E * BITS);  // lanes sharing a word
+    uint32_t part = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) part |= code[e] << (BITS * e);
+    part <<= (E * BITS) * (lane % LPW);
+#pragma unroll
+    for (int off = 1; off < LPW; off <<= 1) part |= __shfl_xor_sync(0xffffffffu, part, off);
+    if (lane % LPW == 0) packed[row * W + lane / LPW] = part;
+  }
+  if ((lane * E) % GS == 0) {
+    const int NG = D / GS;
+    sc[row * NG + (lane * E) / GS] = (uint16_t)sbits;
+    bi[row * NG + (lane * E) / GS] = (uint16_t)bbits;
+  }
+}
+
+template <int BITS, bool F16>
+cudaError_t launch_quant(const float* x, long long rows, int D, int GS, uint32_t* packed, uint16_t* sc, uint16_t* bi,
+                         cudaStream_t s) {
+  const unsigned blocks = (unsigned)((rows + 7) / 8);
+  switch (D) {
+    case 64: qda_quant_kernel<BITS, 2, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi); break;
+    case 128: qda_quant_kernel<BITS, 4, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi); break;
+    case 256: qda_quant_kernel<BITS, 8, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi); break;
+    case 512: qda_quant_kernel<BITS, 16, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace qda
+
+cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool pdl, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.B * p.H));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  switch (out_dtype) {
+    case QDA_BF16: return cudaLaunchKernelEx(&cfg, qda::qda_merge_kernel<QDA_BF16>, p, out);
+    case QDA_FP16: return cudaLaunchKernelEx(&cfg, qda::qda_merge_kernel<QDA_FP16>, p, out);
+    case QDA_FP32: return cudaLaunchKernelEx(&cfg, qda::qda_merge_kernel<QDA_FP32>, p, out);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t qda_launch_quantize(const float* x, long long rows, int D, int GS, int bits, int in_dtype,
+                                uint32_t* packed, uint16_t* scales, uint16_t* biases, cudaStream_t s) {
+  const bool f16 = in_dtype == QDA_FP16;
+  if (bits == 4) {
+    return f16 ? qda::launch_quant<4, true>(x, rows, D, GS, packed, scales, biases, s)
+               : qda::launch_quant<4, false>(x, rows, D, GS, packed, scales, biases, s);
+  }
+  return f16 ? qda::launch_quant<8, true>(x, rows, D, GS, packed, scales, biases, s)
+             : qda::launch_quant<8, false>(x, rows, D, GS, packed, scales, biases, s);
+}

@@ -1,0 +1,371 @@
+// Split kernel of quantized-KV decode attention (sm_103a).
+//
+// One CTA owns one contiguous range of the flattened cache rows (all sequences, all KV heads, back to back) and
+// every query head of the KV heads in that range, so each packed byte is read from HBM exactly once. The flash-
+// decoding split-N of mlx-bun fused-decode-kernel.ts (BLOCK_SOURCE: per-block running max / sum-exp /
+// unnormalised o, merged later) is kept; what changes for GB300:
+//   * the row space is cut into equal ranges, one per resident CTA, instead of fixed blocks per head, so a
+//     ragged batch is balanced across the 152 SMs;
+//   * a producer warp streams each range through a multi-stage shared-memory ring with 1-D bulk copies (TMA)
+//     completing on mbarriers, the consumer warps never touch global memory for K/V;
+//   * the dequantisation is factored out of the dot (SCORE_ROW: sum (s*c + b) q = s * sum c q + b * sum q) and
+//     scores stay fp32, in log2 units (q is pre-scaled by log2(e)/sqrt(D)) so every exponential is one ex2.
+// A range that crosses a (sequence, KV head) boundary ends one segment and starts another; each segment leaves
+// one partial (max, sum, o[D]) per query head in the workspace slot (cta + unit), merged by the merge kernel.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "qda_internal.h"
+#include "qda_ptx.cuh"
+
+namespace qda {
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Iterates the chunks of one CTA's row range. A chunk is the intersection of one pipeline tile (tile_rows rows,
+// aligned in the global row space), one (sequence, KV head) unit and the CTA's range.
+struct ChunkWalker {
+  long long r, r_end, u_start, u_end;
+  int b, kvh, unit;
+
+  __device__ void init(const QdaParams& p, long long r0, long long r1) {
+    r = r0;
+    r_end = r1;
+    int lo = 0, hi = p.B - 1;  // last sequence whose first row is <= r0
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((long long)p.Hkv * p.seq_off[mid] <= r0) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    const long long n = p.seq_off[b + 1] - p.seq_off[b];
+    const long long sb = (long long)p.Hkv * p.seq_off[b];
+    kvh = (int)((r0 - sb) / n);
+    u_start = sb + (long long)kvh * n;
+    u_end = u_start + n;
+    unit = b * p.Hkv + kvh;
+  }
+
+  __device__ bool next(const QdaParams& p, long long& c0, long long& c1, long long& t0) {
+    if (r >= r_end) return false;
+    while (r >= u_end) {
+      if (++kvh == p.Hkv) { kvh = 0; ++b; }
+      const long long n = p.seq_off[b + 1] - p.seq_off[b];
+      u_start = u_end;
+      u_end = u_start + n;
+      unit = b * p.Hkv + kvh;
+    }
+    t0 = (r / p.tile_rows) * p.tile_rows;
+    c0 = r;
+    c1 = min(min(t0 + (long long)p.tile_rows, u_end), r_end);
+    r = c1;
+    return true;
+  }
+};
+
+// Waits for a phase with a time limit but ignores the abort flag: used to let every issued copy land before the
+// CTA exits.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, unsigned int* err) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 1000000000ull) { atomicOr(err, 2u); return; }
+  }
+}
+
+// BITS: 4 or 8. WPL: packed words per lane per row. LPR: lanes per row (RPS = 32/LPR rows per warp step).
+// NH: query heads per CTA. F16: fp16 (else bf16) q / scales / biases. D = LPR * WPL * 32 / BITS.
+template <int BITS, int WPL, int LPR, int NH, bool F16>
+__global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_constant__ QdaParams p) {
+  constexpr int PER = 32 / BITS;          // codes per word
+  constexpr int E = WPL * PER;            // elements per lane per row
+  constexpr int RPS = 32 / LPR;           // rows per warp step
+  constexpr int W = LPR * WPL;            // words per row
+  constexpr int D = W * PER;
+  constexpr uint32_t MASK = (1u << BITS) - 1u;
+  constexpr int NW = QDA_NW;
+
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int TILE = p.tile_rows, STAGES = p.stages, NG = p.NG;
+  const QdaSmemLayout L = qda_smem_layout(TILE, STAGES, W, NG, NH, D);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + STAGES;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
+  float* comb_o = reinterpret_cast<float*>(smem + L.comb);
+  float* comb_m = comb_o + NW * NH * D;
+  float* comb_l = comb_m + NW * NH;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta = blockIdx.x, hc = blockIdx.y;
+  const long long T = p.total_rows;
+  const long long r0 = qda_cta_row(T, p.num_ctas, cta);
+  const long long r1 = qda_cta_row(T, p.num_ctas, cta + 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NW);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  if (r0 >= r1) return;
+
+  ChunkWalker walk;
+  walk.init(p, r0, r1);
+  long long c0, c1, t0;
+
+  if (warp == NW) {
+    // ---------------------------------------------------------------- producer: one lane issues every copy
+    if (lane != 0) return;
+    const uint64_t pol = policy_evict_first();
+    const uint32_t RB = W * 4, SB = NG * 2;
+    int i = 0;
+    while (walk.next(p, c0, c1, t0)) {
+      const int s = i % STAGES;
+      if (i >= STAGES && !mbar_wait_bounded(&empty[s], ((i / STAGES) - 1) & 1, abort_flag, p.err, 1u)) break;
+      unsigned char* st = smem + L.stage0 + (size_t)s * L.stage_bytes;
+      const uint32_t cbytes = (uint32_t)(c1 - c0) * RB;
+      const size_t coff = (size_t)(c0 - t0) * RB;
+      // scales/biases: the 8-row aligned cover of [c0, c1), clipped to the end of the arrays
+      const long long s0 = c0 & ~7LL;
+      const long long s1 = min((c1 + 7) & ~7LL, T);
+      const uint32_t sbytes = (uint32_t)(s1 - s0) * SB;
+      const uint32_t s16 = sbytes & ~15u;
+      const size_t soff = (size_t)(s0 - t0) * SB;
+      const uint16_t* srcs[4] = {p.ks, p.kb, p.vs, p.vb};
+      if (s16 != sbytes) {  // the last (< 16) bytes of the arrays: plain loads, published by the arrive below
+        for (int a = 0; a < 4; ++a) {
+          const uint16_t* src = srcs[a] + s0 * NG + s16 / 2;
+          uint16_t* dst = reinterpret_cast<uint16_t*>(st + 2 * L.codes_bytes + a * L.sc_bytes + soff + s16);
+          for (uint32_t k = 0; k < (sbytes - s16) / 2; ++k) dst[k] = src[k];
+        }
+      }
+      mbar_arrive_expect_tx(&full[s], 2 * cbytes + 4 * s16);
+      bulk_g2s(st + coff, p.kp + c0 * W, cbytes, &full[s], pol);
+      bulk_g2s(st + L.codes_bytes + coff, p.vp + c0 * W, cbytes, &full[s], pol);
+      if (s16) {
+        for (int a = 0; a < 4; ++a)
+          bulk_g2s(st + 2 * L.codes_bytes + a * L.sc_bytes + soff, srcs[a] + s0 * NG, s16, &full[s], pol);
+      }
+      ++i;
+    }
+    for (int j = (i > STAGES ? i - STAGES : 0); j < i; ++j) mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1, p.err);
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int rir = lane / LPR;     // row of the warp step this lane works on
+  const int lir = lane % LPR;     // lane's slice of the row: elements [lir*E, lir*E + E)
+  float qv[NH][E], qsum[NH], o[NH][E], m[NH], l[NH];
+  int cur_unit = -1;
+  int i = 0;
+  while (walk.next(p, c0, c1, t0)) {
+    if (walk.unit != cur_unit) {  // a new (sequence, KV head): load its query heads, reset the softmax state
+      cur_unit = walk.unit;
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const int j = hc * NH + h;
+        float acc = 0.f;
+        if (j < p.nrep) {
+          const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
+                               ((size_t)walk.b * p.H + (size_t)walk.kvh * p.nrep + j) * D + lir * E;
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            qv[h][e] = half_bits_to_float<F16>(qp[e]) * p.qscale;
+            acc += qv[h][e];
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) qv[h][e] = 0.f;
+        }
+        qsum[h] = acc;
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[h][e] = 0.f;
+      }
+    }
+    const int s = i % STAGES;
+    const bool ok = mbar_wait_bounded(&full[s], (i / STAGES) & 1, abort_flag, p.err, 1u);
+    if (ok) {
+      const unsigned char* st = smem + L.stage0 + (size_t)s * L.stage_bytes;
+      const uint32_t* sK = reinterpret_cast<const uint32_t*>(st);
+      const uint32_t* sV = reinterpret_cast<const uint32_t*>(st + L.codes_bytes);
+      const uint16_t* sKS = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes);
+      const uint16_t* sKB = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes + L.sc_bytes);
+      const uint16_t* sVS = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes + 2 * L.sc_bytes);
+      const uint16_t* sVB = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes + 3 * L.sc_bytes);
+      const int g = (lir * E) / p.GS;
+      for (long long rb = c0 + warp * RPS; rb < c1; rb += NW * RPS) {
+        const long long row = rb + rir;
+        const bool valid = row < c1;
+        const int lr = (int)((valid ? row : c0) - t0);
+        // K: factored dot over this lane's slice, then the sum over the LPR lanes of the row
+        float cf[E];
+#pragma unroll
+        for (int w = 0; w < WPL; ++w) {
+          const uint32_t word = sK[lr * W + lir * WPL + w];
+#pragma unroll
+          for (int k = 0; k < PER; ++k)
+            cf[w * PER + k] = __uint_as_float(0x4B000000u | ((word >> (BITS * k)) & MASK)) - 8388608.0f;
+        }
+        const float ksc = half_bits_to_float<F16>(sKS[lr * NG + g]);
+        const float kbi = half_bits_to_float<F16>(sKB[lr * NG + g]);
+        float sc[NH];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          float acc = 0.f;
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc = fmaf(cf[e], qv[h][e], acc);
+          sc[h] = fmaf(ksc, acc, kbi * qsum[h]);
+        }
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+#pragma unroll
+          for (int off = LPR / 2; off >= 1; off >>= 1) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], off);
+        }
+        // online softmax over the rows of this step (one running max per head, shared by the warp)
+        float pr[NH], alpha[NH];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const float sh = valid ? sc[h] : -INFINITY;
+          float mx = sh;
+#pragma unroll
+          for (int off = LPR; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+          const float mn = fmaxf(m[h], mx);
+          if (mn == -INFINITY) {
+            alpha[h] = 1.f;
+            pr[h] = 0.f;
+          } else {
+            alpha[h] = ex2(m[h] - mn);
+            pr[h] = valid ? ex2(sh - mn) : 0.f;
+          }
+          m[h] = mn;
+          l[h] = fmaf(l[h], alpha[h], pr[h]);
+        }
+        // V: o = alpha * o + p * (s * c + b)
+#pragma unroll
+        for (int w = 0; w < WPL; ++w) {
+          const uint32_t word = sV[lr * W + lir * WPL + w];
+#pragma unroll
+          for (int k = 0; k < PER; ++k)
+            cf[w * PER + k] = __uint_as_float(0x4B000000u | ((word >> (BITS * k)) & MASK)) - 8388608.0f;
+        }
+        const float vsc = half_bits_to_float<F16>(sVS[lr * NG + g]);
+        const float vbi = half_bits_to_float<F16>(sVB[lr * NG + g]);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const float ps = pr[h] * vsc, pb = pr[h] * vbi;
+#pragma unroll
+          for (int e = 0; e < E; ++e) o[h][e] = fmaf(o[h][e], alpha[h], fmaf(ps, cf[e], pb));
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+
+    if (c1 == walk.u_end || c1 == r1) {
+      // ------------------------------------------------------------ end of a segment: combine the warps
+      if constexpr (RPS > 1) {
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1) {
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[h][e] += __shfl_xor_sync(0xffffffffu, o[h][e], off);
+          }
+        }
+      }
+      if (rir == 0) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+#pragma unroll
+          for (int e = 0; e < E; ++e) comb_o[(warp * NH + h) * D + lir * E + e] = o[h][e];
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          comb_m[warp * NH + h] = m[h];
+          comb_l[warp * NH + h] = l[h];
+        }
+      }
+      named_barrier_sync(1, NW * 32);
+      const long long slot = (long long)cta + walk.unit;
+      for (int idx = threadIdx.x; idx < NH * D; idx += NW * 32) {
+        const int h = idx / D, d = idx - h * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, comb_m[w * NH + h]);
+        float O = 0.f, Ls = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float mw = comb_m[w * NH + h];
+          const float wt = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+          O = fmaf(comb_o[(w * NH + h) * D + d], wt, O);
+          Ls = fmaf(comb_l[w * NH + h], wt, Ls);
+        }
+        const size_t hp = (size_t)slot * p.heads_pad + (size_t)hc * NH + h;
+        p.part_o[hp * D + d] = O;
+        if (d == 0) p.part_ml[hp] = make_float2(M, Ls);
+      }
+      named_barrier_sync(1, NW * 32);
+    }
+    ++i;
+  }
+}
+
+// Calls f(kernel) with the instantiation for (wpl, lpr, nh); returns cudaErrorInvalidValue for an unbuilt one.
+template <int BITS, bool F16, typename Fn>
+cudaError_t with_split_kernel(int wpl, int lpr, int nh, Fn&& f) {
+#define QDA_NH_CASES(WPL_, LPR_)                                                        \
+  switch (nh) {                                                                         \
+    case 1: return f(qda_split_kernel<BITS, WPL_, LPR_, 1, F16>);                       \
+    case 2: return f(qda_split_kernel<BITS, WPL_, LPR_, 2, F16>);                       \
+    case 4: return f(qda_split_kernel<BITS, WPL_, LPR_, 4, F16>);                       \
+    case 8:                                                                             \
+      if constexpr (WPL_ * (32 / BITS) * 8 <= 64) return f(qda_split_kernel<BITS, WPL_, LPR_, 8, F16>); \
+      else return cudaErrorInvalidValue;                                                \
+    default: return cudaErrorInvalidValue;                                              \
+  }
+  if constexpr (BITS == 4) {
+    if (wpl == 1 && lpr == 8) { QDA_NH_CASES(1, 8) }
+    if (wpl == 1 && lpr == 16) { QDA_NH_CASES(1, 16) }
+    if (wpl == 1 && lpr == 32) { QDA_NH_CASES(1, 32) }
+    if (wpl == 2 && lpr == 32) { QDA_NH_CASES(2, 32) }
+  } else {
+    if (wpl == 1 && lpr == 16) { QDA_NH_CASES(1, 16) }
+    if (wpl == 1 && lpr == 32) { QDA_NH_CASES(1, 32) }
+    if (wpl == 2 && lpr == 32) { QDA_NH_CASES(2, 32) }
+    if (wpl == 4 && lpr == 32) { QDA_NH_CASES(4, 32) }
+  }
+#undef QDA_NH_CASES
+  return cudaErrorInvalidValue;
+}
+
+template <int BITS, bool F16>
+cudaError_t launch_split(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s) {
+  return with_split_kernel<BITS, F16>(wpl, lpr, nh, [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, QDA_THREADS, smem, s>>>(p);
+    return cudaGetLastError();
+  });
+}
+
+template <int BITS, bool F16>
+cudaError_t occupancy_split(int wpl, int lpr, int nh, size_t smem, int* n) {
+  return with_split_kernel<BITS, F16>(wpl, lpr, nh, [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, QDA_THREADS, smem);
+  });
+}
+
+}  // namespace qda

@@ -1,0 +1,11 @@
+// Split-kernel instantiations for 4-bit codes with fp16 q / scales / biases.
+#include "qda_split.cuh"
+
+cudaError_t qda_launch_split_b4_fp16(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem,
+                                       cudaStream_t s) {
+  return qda::launch_split<4, true>(p, wpl, lpr, nh, grid, smem, s);
+}
+
+cudaError_t qda_occupancy_split_b4_fp16(int wpl, int lpr, int nh, size_t smem, int* n) {
+  return qda::occupancy_split<4, true>(wpl, lpr, nh, smem, n);
+}

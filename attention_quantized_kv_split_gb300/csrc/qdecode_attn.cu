@@ -1,0 +1,389 @@
+// Host side of libqdecode_attn: argument checks, the launch plan, workspace handling and the C entry points.
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "qda_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kStages = 4;
+constexpr size_t kStageTarget = 24 * 1024;   // bytes of K+V (codes, scales, biases) per pipeline stage
+constexpr long long kMinRowsPerCta = 128;
+
+thread_local int t_last_cuda_error = 0;
+thread_local void* t_split_event = nullptr;
+std::atomic<int> g_force_splits{0};
+std::atomic<long long> g_calls{0};
+
+__device__ unsigned int g_device_err;
+
+struct DeviceState {
+  std::mutex mu;
+  bool init = false;
+  int num_sms = 0;
+  unsigned int* err = nullptr;      // address of g_device_err on this device
+  void* ws = nullptr;               // library-owned workspace
+  size_t ws_bytes = 0;
+  void* user_ws = nullptr;          // caller-installed workspace
+  size_t user_ws_bytes = 0;
+  std::map<std::tuple<int, int, int, int, int, size_t>, int> occupancy;
+};
+DeviceState g_dev[kMaxDevices];
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return QDA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int pow2ceil(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+// Pure host checks of the shape (no pointers): the support predicate of mlx-bun fused-decode-kernel.ts
+// (fusedDecodeKernelSupported), widened to B >= 1 sequences, any H % Hkv == 0 and fp16 or bf16 input.
+int check_shape(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits) {
+  if (N == nullptr) return QDA_ERR_INVALID;
+  if (B < 1 || H < 1 || Hkv < 1 || D < 1 || GS < 1) return QDA_ERR_INVALID;
+  if (H % Hkv != 0) return QDA_ERR_INVALID;
+  for (int b = 0; b < B && b <= QDA_MAX_B; ++b)
+    if (N[b] < 1) return QDA_ERR_INVALID;
+  if (bits != 4 && bits != 8) return QDA_ERR_UNSUPPORTED;
+  if (GS != 32 && GS != 64 && GS != 128) return QDA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256 && D != 512) return QDA_ERR_UNSUPPORTED;
+  if (D % GS != 0) return QDA_ERR_UNSUPPORTED;
+  if (B > QDA_MAX_B) return QDA_ERR_UNSUPPORTED;
+  if (H / Hkv > QDA_MAX_NREP) return QDA_ERR_UNSUPPORTED;
+  long long total = 0;
+  for (int b = 0; b < B; ++b) total += N[b];
+  if (total > (1LL << 31) - 1) return QDA_ERR_UNSUPPORTED;   // sequence offsets are int32
+  return QDA_OK;
+}
+
+int check_dtype(int dtype, int* in, int* out) {
+  const int i = dtype & 0xff, o = (dtype >> 8) & 0xff;
+  if ((dtype >> 16) != 0) return QDA_ERR_INVALID;
+  if (i != QDA_BF16 && i != QDA_FP16) return QDA_ERR_INVALID;
+  if (o != 0 && o != QDA_BF16 && o != QDA_FP16 && o != QDA_FP32) return QDA_ERR_INVALID;
+  *in = i;
+  *out = o == 0 ? i : o;
+  return QDA_OK;
+}
+
+struct Variant {
+  int W, wpl, lpr, E, nh, hc, heads_pad, NG, tile, stages;
+  size_t smem;
+};
+
+Variant pick_variant(int H, int Hkv, int D, int GS, int bits) {
+  Variant v;
+  v.W = D * bits / 32;
+  v.wpl = v.W > 32 ? v.W / 32 : 1;
+  v.lpr = v.W > 32 ? 32 : v.W;
+  v.E = v.wpl * (32 / bits);
+  const int nrep = H / Hkv;
+  const int nh_max = std::min(8, 64 / v.E);
+  v.nh = std::min(pow2ceil(nrep), nh_max);
+  v.hc = (nrep + v.nh - 1) / v.nh;
+  v.heads_pad = v.hc * v.nh;
+  v.NG = D / GS;
+  const size_t row_bytes = 2 * (size_t)v.W * 4 + 4 * (size_t)v.NG * 2;
+  int tile = 256;
+  while (tile > 16 && (size_t)tile * row_bytes > kStageTarget) tile >>= 1;
+  v.tile = tile;
+  v.stages = kStages;
+  v.smem = qda_smem_layout(v.tile, v.stages, v.W, v.NG, v.nh, D).total;
+  return v;
+}
+
+cudaError_t split_occupancy(int bits, bool f16, const Variant& v, int* n) {
+  if (bits == 4) {
+    return f16 ? qda_occupancy_split_b4_fp16(v.wpl, v.lpr, v.nh, v.smem, n)
+               : qda_occupancy_split_b4_bf16(v.wpl, v.lpr, v.nh, v.smem, n);
+  }
+  return f16 ? qda_occupancy_split_b8_fp16(v.wpl, v.lpr, v.nh, v.smem, n)
+             : qda_occupancy_split_b8_bf16(v.wpl, v.lpr, v.nh, v.smem, n);
+}
+
+cudaError_t split_launch(int bits, bool f16, const QdaParams& p, const Variant& v, dim3 grid, cudaStream_t s) {
+  if (bits == 4) {
+    return f16 ? qda_launch_split_b4_fp16(p, v.wpl, v.lpr, v.nh, grid, v.smem, s)
+               : qda_launch_split_b4_bf16(p, v.wpl, v.lpr, v.nh, grid, v.smem, s);
+  }
+  return f16 ? qda_launch_split_b8_fp16(p, v.wpl, v.lpr, v.nh, grid, v.smem, s)
+             : qda_launch_split_b8_bf16(p, v.wpl, v.lpr, v.nh, grid, v.smem, s);
+}
+
+// The plan: one contiguous, equal share of the flattened rows per CTA, as many CTAs as fit on the GPU at once
+// (one wave), but no fewer than kMinRowsPerCta rows each. Deterministic in (shape, SM count, occupancy).
+void make_plan(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int num_sms, int ctas_per_sm,
+               const Variant& v, qda_plan* plan) {
+  long long sumN = 0;
+  for (int b = 0; b < B; ++b) sumN += N[b];
+  const long long T = (long long)Hkv * sumN;
+  const int units = B * Hkv;
+  long long target = std::max(1LL, (long long)num_sms * std::max(1, ctas_per_sm) / v.hc);
+  long long by_rows = std::max(1LL, (T + kMinRowsPerCta - 1) / kMinRowsPerCta);
+  long long C = std::min(target, by_rows);
+  const int forced = g_force_splits.load();
+  if (forced > 0) C = forced;
+  C = std::min<long long>(C, 1 << 20);
+  plan->num_ctas = (int)C;
+  plan->head_chunks = v.hc;
+  plan->heads_per_cta = v.nh;
+  plan->tile_rows = v.tile;
+  plan->stages = v.stages;
+  plan->threads = QDA_THREADS;
+  plan->units = units;
+  plan->smem_bytes = (int)v.smem;
+  plan->total_rows = T;
+  plan->slots = C + units;
+  const size_t o_bytes = (size_t)plan->slots * v.heads_pad * D * sizeof(float);
+  const size_t ml_bytes = (size_t)plan->slots * v.heads_pad * 2 * sizeof(float);
+  plan->workspace_bytes = ((o_bytes + 255) & ~(size_t)255) + ml_bytes;
+  (void)GS;
+  (void)bits;
+}
+
+DeviceState* device_state(int* dev_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    t_last_cuda_error = (int)e;
+    return nullptr;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceState& d = g_dev[dev];
+  std::lock_guard<std::mutex> lock(d.mu);
+  if (!d.init) {
+    if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_device_err)) != cudaSuccess) {
+      t_last_cuda_error = (int)e;
+      return nullptr;
+    }
+    d.init = true;
+  }
+  *dev_out = dev;
+  return &d;
+}
+
+int occupancy_for(DeviceState& d, int bits, bool f16, const Variant& v, int* n) {
+  std::lock_guard<std::mutex> lock(d.mu);
+  auto key = std::make_tuple(bits, (int)f16, v.wpl, v.lpr, v.nh, v.smem);
+  auto it = d.occupancy.find(key);
+  if (it != d.occupancy.end()) {
+    *n = it->second;
+    return QDA_OK;
+  }
+  cudaError_t e = split_occupancy(bits, f16, v, n);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (*n < 1) *n = 1;
+  d.occupancy[key] = *n;
+  return QDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qdecode_attn_plan(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int num_sms,
+                      int ctas_per_sm, qda_plan* plan) {
+  if (plan == nullptr) return QDA_ERR_INVALID;
+  int st = check_shape(B, H, Hkv, N, D, GS, bits);
+  if (st != QDA_OK) return st;
+  const Variant v = pick_variant(H, Hkv, D, GS, bits);
+  if (num_sms <= 0 || ctas_per_sm <= 0) {
+    int dev;
+    DeviceState* d = device_state(&dev);
+    if (d == nullptr) return QDA_ERR_CUDA;
+    if (num_sms <= 0) num_sms = d->num_sms;
+    if (ctas_per_sm <= 0) {
+      // the input dtype does not change the kernel's resources; bf16 stands for both
+      st = occupancy_for(*d, bits, false, v, &ctas_per_sm);
+      if (st != QDA_OK) return st;
+    }
+  }
+  make_plan(B, H, Hkv, N, D, GS, bits, num_sms, ctas_per_sm, v, plan);
+  return QDA_OK;
+}
+
+int qdecode_attn_workspace_bytes(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, size_t* bytes) {
+  if (bytes == nullptr) return QDA_ERR_INVALID;
+  qda_plan plan;
+  const int st = qdecode_attn_plan(B, H, Hkv, N, D, GS, bits, 0, 0, &plan);
+  if (st != QDA_OK) return st;
+  *bytes = plan.workspace_bytes;
+  return QDA_OK;
+}
+
+int qdecode_attn_set_workspace(void* ptr, size_t bytes) {
+  if (ptr != nullptr && !aligned16(ptr)) return QDA_ERR_ALIGN;
+  int dev;
+  DeviceState* d = device_state(&dev);
+  if (d == nullptr) return QDA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(d->mu);
+  d->user_ws = ptr;
+  d->user_ws_bytes = ptr ? bytes : 0;
+  return QDA_OK;
+}
+
+int qdecode_attn_debug_force_splits(int num_ctas) {
+  if (num_ctas < 0) return QDA_ERR_INVALID;
+  g_force_splits.store(num_ctas);
+  return QDA_OK;
+}
+
+int qdecode_attn_set_split_event(void* event) {
+  t_split_event = event;
+  return QDA_OK;
+}
+
+int qdecode_attn(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
+                 const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out, int B, int H,
+                 int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream) {
+  if (!q || !k_packed || !k_scales || !k_biases || !v_packed || !v_scales || !v_biases || !out)
+    return QDA_ERR_INVALID;
+  int in_dt, out_dt;
+  int st = check_dtype(dtype, &in_dt, &out_dt);
+  if (st != QDA_OK) return st;
+  st = check_shape(B, H, Hkv, N, D, GS, bits);
+  if (st != QDA_OK) return st;
+  const void* ptrs[8] = {q, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return QDA_ERR_ALIGN;
+
+  int dev;
+  DeviceState* d = device_state(&dev);
+  if (d == nullptr) return QDA_ERR_CUDA;
+  const bool f16 = in_dt == QDA_FP16;
+  const Variant v = pick_variant(H, Hkv, D, GS, bits);
+  int occ = 1;
+  st = occupancy_for(*d, bits, f16, v, &occ);
+  if (st != QDA_OK) return st;
+  qda_plan plan;
+  make_plan(B, H, Hkv, N, D, GS, bits, d->num_sms, occ, v, &plan);
+
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(d->mu);
+    if (d->user_ws != nullptr) {
+      if (d->user_ws_bytes < plan.workspace_bytes) return QDA_ERR_WORKSPACE;
+      ws = d->user_ws;
+    } else {
+      if (d->ws_bytes < plan.workspace_bytes) {
+        if (d->ws != nullptr) cudaFree(d->ws);
+        d->ws = nullptr;
+        d->ws_bytes = 0;
+        const size_t want = std::max(plan.workspace_bytes, (size_t)1 << 20);
+        cudaError_t e = cudaMalloc(&d->ws, want);
+        if (e != cudaSuccess) return cuda_fail(e);
+        d->ws_bytes = want;
+      }
+      ws = d->ws;
+    }
+  }
+
+  QdaParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q;
+  p.kp = k_packed;
+  p.ks = static_cast<const uint16_t*>(k_scales);
+  p.kb = static_cast<const uint16_t*>(k_biases);
+  p.vp = v_packed;
+  p.vs = static_cast<const uint16_t*>(v_scales);
+  p.vb = static_cast<const uint16_t*>(v_biases);
+  const size_t o_bytes = (size_t)plan.slots * v.heads_pad * D * sizeof(float);
+  p.part_o = static_cast<float*>(ws);
+  p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + ((o_bytes + 255) & ~(size_t)255));
+  p.err = d->err;
+  p.total_rows = plan.total_rows;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.GS = GS;
+  p.NG = v.NG;
+  p.W = v.W;
+  p.nrep = H / Hkv;
+  p.heads_pad = v.heads_pad;
+  p.num_ctas = plan.num_ctas;
+  p.tile_rows = v.tile;
+  p.stages = v.stages;
+  p.qscale = 1.4426950408889634f / sqrtf((float)D);
+  p.seq_off[0] = 0;
+  for (int b = 0; b < B; ++b) p.seq_off[b + 1] = p.seq_off[b] + N[b];
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = split_launch(bits, f16, p, v, dim3((unsigned)plan.num_ctas, (unsigned)v.hc), s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const bool use_event = t_split_event != nullptr;
+  if (use_event) {
+    e = cudaEventRecord(static_cast<cudaEvent_t>(t_split_event), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  e = qda_launch_merge(p, out, out_dt, !use_event, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_calls.fetch_add(1);
+  return QDA_OK;
+}
+
+int qdecode_quantize(const float* x, long long rows, int D, int GS, int bits, int dtype, uint32_t* packed,
+                     void* scales, void* biases, void* stream) {
+  if (!x || !packed || !scales || !biases) return QDA_ERR_INVALID;
+  if (rows < 1 || D < 1 || GS < 1) return QDA_ERR_INVALID;
+  int in_dt, out_dt;
+  int st = check_dtype(dtype, &in_dt, &out_dt);
+  if (st != QDA_OK) return st;
+  if (bits != 4 && bits != 8) return QDA_ERR_UNSUPPORTED;
+  if (GS != 32 && GS != 64 && GS != 128) return QDA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256 && D != 512) return QDA_ERR_UNSUPPORTED;
+  if (D % GS != 0) return QDA_ERR_UNSUPPORTED;
+  if (rows > (1LL << 31) * 8 - 8) return QDA_ERR_UNSUPPORTED;
+  if (((uintptr_t)x & 15u) || ((uintptr_t)packed & 3u) || ((uintptr_t)scales & 1u) || ((uintptr_t)biases & 1u))
+    return QDA_ERR_ALIGN;
+  cudaError_t e = qda_launch_quantize(x, rows, D, GS, bits, in_dt, packed, static_cast<uint16_t*>(scales),
+                                      static_cast<uint16_t*>(biases), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return QDA_OK;
+}
+
+const char* qdecode_attn_strerror(int status) {
+  switch (status) {
+    case QDA_OK: return "success";
+    case QDA_ERR_INVALID: return "invalid argument (null pointer, non-positive size, H % Hkv != 0, N[b] < 1 or bad dtype)";
+    case QDA_ERR_UNSUPPORTED: return "unsupported shape (bits, GS, D, B or H/Hkv outside the built variants)";
+    case QDA_ERR_ALIGN: return "a data pointer is not 16-byte aligned";
+    case QDA_ERR_CUDA: return "CUDA runtime error (see qdecode_attn_last_cuda_error)";
+    case QDA_ERR_WORKSPACE: return "installed workspace is too small for this call";
+    default: return "unknown status";
+  }
+}
+
+int qdecode_attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+int qdecode_attn_device_status(unsigned int* flags) {
+  if (flags == nullptr) return QDA_ERR_INVALID;
+  int dev;
+  DeviceState* d = device_state(&dev);
+  if (d == nullptr) return QDA_ERR_CUDA;
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_err, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e);
+  const unsigned int zero = 0;
+  e = cudaMemcpyToSymbol(g_device_err, &zero, sizeof(zero));
+  if (e != cudaSuccess) return cuda_fail(e);
+  *flags = v;
+  return QDA_OK;
+}
+
+long long qdecode_attn_calls(void) { return g_calls.load(); }
+
+}  // extern "C"

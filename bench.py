@@ -1,0 +1,447 @@
+#!/usr/bin/env python
+"""Benchmark of quantized-KV single-query decode attention on GB300.
+
+One step = one qdecode_attn call (split kernel + merge kernel) over the whole synthetic workload, the 8k case by
+default: B=1, H=16, Hkv=8, D=256, N=8192, 8-bit affine KV in groups of 32, bf16 q and output. The cache is resident
+in HBM; L2 is flushed (a 2 x L2-size write) before every timed call, outside the call's events. The metric is KV
+bytes per call (packed codes + scales + biases of K and V, each read once) over the call's device time.
+
+    python bench.py [--steps K] [--warmup W] [--workload 1..5] [--impl ours|reference] [--no-extra]
+
+Prints one JSON line. Under torchrun (N > 1) every rank runs an independent replica on its own GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+if "reference" in sys.argv:
+    # the reference arm times the single-threaded oracle: pin BLAS to one thread before numpy loads
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_v] = "1"
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized-KV decode attn: KV-bytes GB/s vs HBM peak; µs/call @8k"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--no-extra", action="store_true", help="skip the per-workload figures for workloads 3-5")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def kv_bytes(w, N) -> int:
+    rows = w.Hkv * sum(N)
+    W, NG = w.D * w.bits // 32, w.D // w.GS
+    return 2 * rows * (W * 4 + 2 * NG * 2)
+
+
+def config_of(w, N, extra=None) -> dict:
+    c = {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "D": w.D, "bits": w.bits, "GS": w.GS,
+         "N": N if len(N) <= 8 else f"{len(N)} sequences", "dtype_in": w.dtype_in, "dtype_out": w.dtype_out,
+         "kv_bytes_per_call": kv_bytes(w, N), "parallelism": "replicas",
+         "l2": "flushed before every timed call (write of 2 x L2 bytes, outside the call's events)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def split_kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("qda_split.cuh", "qda_ptx.cuh", "qda_internal.h", "qdecode_attn.cu"):
+        with open(os.path.join(ROOT, "attention_quantized_kv_split_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch of the split kernel from the committed ncu summary, if it matches this source."""
+    path = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload_name)
+        if e and e.get("kernel_hash") == split_kernel_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons every 100 ms, each line stamped on arrival."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for s in self.samples if t0 <= s[0] <= t1 + 0.15]
+        if not inside and self.samples:
+            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:2]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, p in inside:
+            for k, nm in enumerate(names):
+                if p[5 + k].lower().startswith("active"):
+                    reasons.add(nm)
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for _, p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for _, p in inside if num(p[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside),
+                "power_w_max": max((num(p[3]) or 0.0) for _, p in inside)}
+
+
+# --------------------------------------------------------------------------------------------- our arm
+
+
+def make_workload(w, device):
+    import torch
+    import attention_quantized_kv_split_gb300 as qda
+    from attention_quantized_kv_split_gb300 import synth
+    N = synth.lengths(w)
+    q = synth.query(w)
+    cache = qda.QuantizedKV.empty(N, w.Hkv, w.D, w.GS, w.bits, synth.DT[w.dtype_in], device=device)
+    for b in range(w.B):
+        for kvh in range(w.Hkv):
+            K, V = synth.kv_unit(w, b, kvh, N[b], q=q, device=device)
+            cache.quantize_into(b, kvh, K, V)
+            del K, V
+    torch.cuda.synchronize()
+    return N, q.to(device), cache
+
+
+def time_calls(fn, steps, flush, stream):
+    """Per-call device time (ms) with L2 flushed before each call, events on the launching stream."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for k in range(steps):
+        flush()
+        starts[k].record(stream)
+        fn()
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def cpu_oracle_unit(args):
+    import numpy as np
+    import oracle as O
+    qh, kp, ks, kb, vp, vs, vb, D, GS, bits = args
+    Kd = O.dequantize(O.unpack(kp, bits, D), ks, kb, GS)
+    Vd = O.dequantize(O.unpack(vp, bits, D), vs, vb, GS)
+    return [O.attention_head(qh[j], Kd, Vd) for j in range(qh.shape[0])]
+
+
+def cpu_baseline(w, N, q, cache, pool):
+    """The oracle, unchanged, on the host cores: one spawned single-threaded worker per (sequence, KV head)."""
+    import numpy as np
+    items = []
+    nbytes = 0
+    qv = q.double().cpu().numpy()
+    max_units = 16
+    for b in range(w.B):
+        for kvh in range(w.Hkv):
+            if len(items) >= max_units:
+                break
+            r0, r1 = cache.unit_rows(b, kvh)
+            arrs = [cache.kp[r0:r1].cpu().numpy().view(np.uint32), cache.ks[r0:r1].float().cpu().numpy(),
+                    cache.kb[r0:r1].float().cpu().numpy(), cache.vp[r0:r1].cpu().numpy().view(np.uint32),
+                    cache.vs[r0:r1].float().cpu().numpy(), cache.vb[r0:r1].float().cpu().numpy()]
+            items.append((qv[b, kvh * w.nrep:(kvh + 1) * w.nrep], *arrs, w.D, w.GS, w.bits))
+            nbytes += sum(a.nbytes for a in arrs[:1] + arrs[3:4]) + 2 * sum(a.size for a in arrs[1:3] + arrs[4:6])
+    total_units = w.B * w.Hkv
+    t0 = time.perf_counter()
+    pool.map(cpu_oracle_unit, items)
+    dt = time.perf_counter() - t0
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": pool._processes, "kind": "oracle",
+            "sample": f"{len(items)} of {total_units} (sequence, KV head) units of {w.name}, all their query heads; "
+                      f"one single-threaded worker process per unit", "seconds": dt}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import attention_quantized_kv_split_gb300 as qda
+    from attention_quantized_kv_split_gb300 import build, synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pool = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the oracle's worker pool is spawned before the first GPU call
+        import multiprocessing as mp
+        os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+        ctx = mp.get_context("spawn")
+        pool = ctx.Pool(processes=max(1, min(16, os.cpu_count() or 1)))
+        pool.map(abs, range(pool._processes))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    build.build()
+    qda.lib()
+    stream = torch.cuda.current_stream()
+
+    w = synth.workload(args.workload)
+    N, q, cache = make_workload(w, device)
+    out = torch.empty((w.B, w.H, w.D), dtype=synth.DT[w.dtype_out], device=device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+
+    def flush():
+        flush_buf.zero_()
+
+    def call():
+        qda.decode_attention(q, cache, out=out)
+
+    plan = qda.qdecode_attn_plan(w.B, w.H, w.Hkv, N, w.D, w.GS, w.bits)
+    for _ in range(max(3, args.warmup)):
+        flush()
+        call()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.25 if sampler else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    calls_before = qda.qdecode_attn_calls()
+    ms = time_calls(call, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t1 = time.time()
+    launches = 2 * (qda.qdecode_attn_calls() - calls_before)
+    clocks = sampler.summary(t0, t1) if sampler else None
+    if sampler:
+        sampler.stop()
+    dev_ms_total = sum(ms)
+    if world > 1:
+        tt = torch.tensor([dev_ms_total], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        dev_ms_total = float(tt.item())
+    nbytes = kv_bytes(w, N)
+    ms_per_step = dev_ms_total / args.steps
+    value = world * nbytes * args.steps / (dev_ms_total * 1e-3) / 1e9
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    # dominant kernel: the split kernel, timed alone via an event recorded between the two launches
+    rsteps = min(args.steps, 300)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(rsteps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(rsteps)]
+    ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(rsteps)]
+    for k in range(rsteps):
+        flush()
+        ev0[k].record(stream)
+        qda.qdecode_attn_set_split_event(ev1[k])
+        call()
+        qda.qdecode_attn_set_split_event(None)
+        ev2[k].record(stream)
+    torch.cuda.synchronize()
+    split_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev0, ev1))
+    merge_ms = statistics.mean(b.elapsed_time(c) for b, c in zip(ev1, ev2))
+    peak, peak_kind = measured_peaks()
+    achieved = nbytes / (split_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
+                "kernel": "qda_split_kernel", "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6800 GB/s",
+                "split_kernel_us": round(split_ms * 1e3, 3), "merge_kernel_us": round(merge_ms * 1e3, 3),
+                "algorithmic_bytes_per_launch": nbytes}
+
+    # end to end through the public API with host buffers: H2D of q and the whole cache, the call, D2H of out
+    esteps = min(args.steps, 100)
+    hq = q.cpu().pin_memory()
+    host = [t.cpu().pin_memory() for t in (cache.kp, cache.ks, cache.kb, cache.vp, cache.vs, cache.vb)]
+    dev = [torch.empty_like(t) for t in (cache.kp, cache.ks, cache.kb, cache.vp, cache.vs, cache.vb)]
+    dq = torch.empty_like(q)
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    h2d = hq.numel() * hq.element_size() + sum(t.numel() * t.element_size() for t in host)
+    d2h = hout.numel() * hout.element_size()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(esteps):
+        dq.copy_(hq, non_blocking=True)
+        for d_, h_ in zip(dev, host):
+            d_.copy_(h_, non_blocking=True)
+        qda.qdecode_attn(dq, *dev, out, N, w.Hkv, w.GS, w.bits)
+        hout.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / esteps
+    e2e = {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": esteps}
+
+    extra = {}
+    if not args.no_extra:
+        for idx in (3, 4, 5):
+            if idx == args.workload:
+                continue
+            wx = synth.workload(idx)
+            Nx, qx, cx = make_workload(wx, device)
+            ox = torch.empty((wx.B, wx.H, wx.D), dtype=synth.DT[wx.dtype_out], device=device)
+            fx = lambda: qda.decode_attention(qx, cx, out=ox)  # noqa: E731
+            for _ in range(5):
+                fx()
+            msx = time_calls(fx, 50, flush, stream)
+            bx = kv_bytes(wx, Nx)
+            mx = statistics.median(msx)
+            extra[wx.name] = {"us_per_call": round(mx * 1e3, 2), "kv_GBps": round(bx / (mx * 1e-3) / 1e9, 1),
+                              "frac_of_peak": round(bx / (mx * 1e-3) / 1e9 / peak, 4), "kv_bytes": bx}
+            del cx, qx, ox
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if pool is not None:
+        cpu = cpu_baseline(w, N, q, cache, pool)
+        pool.close()
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "us_per_call": round(ms_per_step * 1e3, 3),
+            "us_per_call_median": round(statistics.median(ms) * 1e3, 3),
+            "wall_ms_per_step": round((t1 - t0) * 1e3 / args.steps, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 (codes u4/u8, q bf16)"
+            if w.dtype_in == "bf16" else "f32 (codes u4/u8, q fp16)",
+            "data": "synthetic (seeded generator; K, V ~ N(0,1) fp32 quantized by the library)",
+            "config": config_of(w, N, {"plan": plan}), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks, "per_workload": extra, "impl": "ours"}
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------------------- reference arm
+
+
+def run_reference(args):
+    """The oracle as it stands, single-threaded on a host core, over a bounded sample of the same workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    import oracle as O
+    from attention_quantized_kv_split_gb300 import synth
+
+    w = synth.workload(args.workload)
+    N = synth.lengths(w)
+    q = synth.query(w)
+    # one (sequence, KV head) unit, quantized by the oracle itself from the same generator (CPU stream)
+    K, V = synth.kv_unit(w, 0, 0, N[0], q=q)
+    kp, ks, kb, vp, vs, vb = O.quantize_cache(K.numpy(), V.numpy(), w.GS, w.bits, w.dtype_in)
+    qh = q.double().numpy()[0, :w.nrep]
+    W, NG = w.D * w.bits // 32, w.D // w.GS
+    row_bytes = 2 * (W * 4 + 2 * NG * 2)
+
+    def step(rows):
+        Kd = O.dequantize(O.unpack(kp[:rows], w.bits, w.D), ks[:rows], kb[:rows], w.GS)
+        Vd = O.dequantize(O.unpack(vp[:rows], w.bits, w.D), vs[:rows], vb[:rows], w.GS)
+        for j in range(w.nrep):
+            O.attention_head(qh[j], Kd, Vd)
+
+    # size each step so that warm-up + steps take about 90 s in all
+    t = time.perf_counter()
+    step(N[0])
+    per_row = (time.perf_counter() - t) / N[0]
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    rows = int(max(16, min(N[0], budget / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        step(rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(rows)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = rows * row_bytes / dt / 1e9
+    sample = (f"{rows} rows of one (sequence, KV head) unit of {w.name} with its {w.nrep} query heads per step "
+              f"(the full call is {w.B * w.Hkv} units of {N[0] if w.B == 1 else 'ragged'} rows)")
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator)",
+            "config": config_of(w, N), "impl": "reference",
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,149 @@
+/*
+ * qdecode_attn.h - single-query (L = 1) decode attention read straight from an affine-quantized KV cache,
+ * on one NVIDIA GB300 (sm_103a). C ABI: plain pointers and sizes, no framework types.
+ *
+ * The operation (mlx-bun fused-decode-kernel.ts, header comment, fusedDecodeSdpa and MERGE_SOURCE; maya-mac
+ * mlx_kernels.py, _ATTEND for the 1/sqrt(D) scale): for every sequence b and query head h, with KV head
+ * kv = h / (H / Hkv),
+ *
+ *     out[b, h, :] = sum_n softmax_n( q[b, h, :] . k_hat[b, kv, n, :] / sqrt(D) ) * v_hat[b, kv, n, :]
+ *
+ * where k_hat = scale * code + bias per group of GS consecutive elements along D (maya-mac _linear_kernel 8-bit
+ * load; fused-decode-kernel.ts SCORE_ROW). The dequantised cache and the score row are never written to
+ * memory: the library streams the packed rows once, splits the rows of the whole batch into equal contiguous
+ * ranges (one per CTA), keeps an online softmax per range and merges the ranges in a fixed order (flash-
+ * decoding split-N, fused-decode-kernel.ts BLOCK_SOURCE / MERGE_SOURCE). Results are bitwise reproducible
+ * from run to run for a given shape and GPU.
+ *
+ * Cache format (MLX affine quantization):
+ *   packed  uint32 words, 32/bits codes per word, least-significant code first: element i of a row is
+ *           (word[i / (32/bits)] >> (bits * (i % (32/bits)))) & (2^bits - 1).
+ *   scales, biases  one per group of GS elements, stored in the input dtype (bf16 or fp16).
+ *
+ * Layouts (row-major, all device memory owned by the caller):
+ *   q       [B, H, D]                     input dtype
+ *   out     [B, H, D]                     output dtype
+ *   per sequence b, back to back with no padding, starting at row Hkv * (N[0] + ... + N[b-1]):
+ *     k_packed, v_packed  [Hkv, N[b], D * bits / 32]  uint32
+ *     k_scales, k_biases, v_scales, v_biases  [Hkv, N[b], D / GS]  input dtype
+ *   For B = 1 this is MLX's [1, Hkv, N, .] cache layout.
+ *
+ * Error behaviour: every function returns a status (0 = success, negative = QDA_ERR_*). Arguments are checked
+ * on the host before anything is launched; a rejected call touches no GPU state. Nothing aborts, throws across
+ * the ABI or traps on the device. A CUDA runtime error is returned as QDA_ERR_CUDA and kept for
+ * qdecode_attn_last_cuda_error() (per host thread).
+ */
+#ifndef QDECODE_ATTN_H
+#define QDECODE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QDA_OK 0
+#define QDA_ERR_INVALID (-1)     /* null pointer, non-positive size, H % Hkv != 0, N[b] < 1, bad dtype code */
+#define QDA_ERR_UNSUPPORTED (-2) /* bits not in {4, 8}, GS not in {32, 64, 128}, D not in {64, 128, 256, 512},
+                                    D % GS != 0, B > QDA_MAX_B, H / Hkv > QDA_MAX_NREP */
+#define QDA_ERR_ALIGN (-3)       /* a data pointer is not 16-byte aligned */
+#define QDA_ERR_CUDA (-4)        /* CUDA runtime error; see qdecode_attn_last_cuda_error() */
+#define QDA_ERR_WORKSPACE (-5)   /* the caller-provided workspace is smaller than the call needs */
+
+#define QDA_BF16 1
+#define QDA_FP16 2
+#define QDA_FP32 3
+/* dtype argument: input dtype (of q, scales and biases) in the low byte, output dtype in the next byte; an
+   output byte of 0 means "same as the input". Input: QDA_BF16 or QDA_FP16. Output: any of the three. */
+#define QDA_DTYPE(in_, out_) ((in_) | ((out_) << 8))
+
+#define QDA_MAX_B 512
+#define QDA_MAX_NREP 64
+
+/*
+ * qdecode_attn: decode attention for B sequences (the operation above). Asynchronous on `stream` (a
+ * cudaStream_t; NULL = the legacy default stream): returns once the two kernels are enqueued and never
+ * synchronises. N is a HOST array of B lengths (N[b] >= 1). The call reads q and the cache, writes out, and uses
+ * a workspace of qdecode_attn_workspace_bytes() bytes: the library's own per-device buffer (allocated or grown
+ * with cudaMalloc on first need, which synchronises the device) unless one was installed with
+ * qdecode_attn_set_workspace(). Calls that share one workspace must not overlap on the GPU.
+ */
+int qdecode_attn(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
+                 const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out,
+                 int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream);
+
+/* The launch plan qdecode_attn would use (host only). Determined by the shape and the GPU alone. */
+typedef struct {
+  int num_ctas;           /* CTAs along the flattened row space (each takes one contiguous row range) */
+  int head_chunks;        /* CTAs per row range when one CTA cannot hold all H/Hkv query heads of a KV head */
+  int heads_per_cta;      /* query heads a CTA serves (H/Hkv rounded up to a power of two, capped) */
+  int tile_rows;          /* cache rows per pipeline stage */
+  int stages;             /* pipeline depth (stages of tile_rows rows in flight per CTA) */
+  int threads;            /* threads per CTA */
+  int units;              /* B * Hkv (sequence, KV head) pairs */
+  int smem_bytes;         /* dynamic shared memory per CTA */
+  long long total_rows;   /* Hkv * (N[0] + ... + N[B-1]) */
+  long long slots;        /* partial-result slots in the workspace */
+  size_t workspace_bytes;
+} qda_plan;
+
+/*
+ * qdecode_attn_plan: fill *plan for this shape. num_sms / ctas_per_sm describe the GPU; pass 0 for either to
+ * query the current device (that needs a GPU). Same argument checks and status codes as qdecode_attn.
+ */
+int qdecode_attn_plan(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int num_sms,
+                      int ctas_per_sm, qda_plan* plan);
+
+/* Workspace size in bytes qdecode_attn needs for this shape on the current device. */
+int qdecode_attn_workspace_bytes(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, size_t* bytes);
+
+/*
+ * Install a caller-owned device workspace for the current device (16-byte aligned; ptr = NULL reverts to the
+ * library's own buffer). The library never frees it. A call whose shape needs more returns QDA_ERR_WORKSPACE.
+ */
+int qdecode_attn_set_workspace(void* ptr, size_t bytes);
+
+/*
+ * Testing aid: force the number of row-range CTAs (0 = use the heuristic). Applies to later calls from every
+ * thread. Results stay within the oracle tolerance for any split count; bitwise identity holds per split count.
+ */
+int qdecode_attn_debug_force_splits(int num_ctas);
+
+/*
+ * Timing aid: when `event` (a cudaEvent_t) is non-NULL, later qdecode_attn calls from this host thread record it
+ * on the stream between the split kernel and the merge kernel (the merge then launches without programmatic
+ * dependent launch). NULL switches it off.
+ */
+int qdecode_attn_set_split_event(void* event);
+
+/*
+ * qdecode_quantize: quantize `rows` fp32 rows x [rows, D] (device) into the cache format above and write
+ * packed [rows, D*bits/32] uint32, scales and biases [rows, D/GS] in the input dtype of `dtype`. Per group:
+ * scale = (max - min) / (2^bits - 1) and bias = min, both computed in fp32 and stored rounded to nearest-even;
+ * code = clamp(rint((x - bias) / scale), 0, 2^bits - 1) in IEEE fp32 (code 0 where the stored scale is 0).
+ * Appending new tokens to a cache is this call on pointers offset to the first new row. Asynchronous on stream.
+ */
+int qdecode_quantize(const float* x, long long rows, int D, int GS, int bits, int dtype, uint32_t* packed,
+                     void* scales, void* biases, void* stream);
+
+/* Human-readable text for a status code (static storage). */
+const char* qdecode_attn_strerror(int status);
+
+/* The cudaError_t behind the last QDA_ERR_CUDA returned on this host thread (0 if none). */
+int qdecode_attn_last_cuda_error(void);
+
+/*
+ * Device-side status: copies (synchronously) and clears the current device's error word. Bits: 1 = a pipeline
+ * wait in the split kernel gave up after its time limit (the output of that call is invalid). 0 = clean.
+ */
+int qdecode_attn_device_status(unsigned int* flags);
+
+/* Number of qdecode_attn calls that launched kernels since the library was loaded (all threads). */
+long long qdecode_attn_calls(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QDECODE_ATTN_H */

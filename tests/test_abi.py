@@ -1,0 +1,170 @@
+"""The C ABI without a GPU: the library loads, exports what the header declares, rejects bad arguments before any
+launch, and plans deterministically. No call here reaches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_quantized_kv_split_gb300 import _lib, build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    qbuild.build()
+    return _lib.lib()
+
+
+def header_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w \*]*?\b(qdecode_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = header_functions()
+    assert "qdecode_attn" in names and "qdecode_quantize" in names and len(names) >= 10
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in header_functions():
+        assert hasattr(L, name), name
+        assert name in _lib.SIGNATURES, f"{name} has no ctypes signature"
+
+
+FAKE = 0x7F0000000000  # never dereferenced: every call below fails its host-side checks first
+
+
+def call(L, B=1, H=8, Hkv=2, N=(512,), D=256, GS=64, bits=4, dtype=1, ptrs=None, nptr=None):
+    p = [FAKE + 256 * i for i in range(8)] if ptrs is None else ptrs
+    n = _lib.int32_array(N) if nptr is None else nptr
+    return L.qdecode_attn(*p, B, H, Hkv, n, D, GS, bits, dtype, None)
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_null_pointer_is_invalid(L, i):
+    p = [FAKE + 256 * k for k in range(8)]
+    p[i] = None
+    assert call(L, ptrs=p) == _lib.QDA_ERR_INVALID
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_misaligned_pointer(L, i):
+    p = [FAKE + 256 * k for k in range(8)]
+    p[i] += 8
+    assert call(L, ptrs=p) == _lib.QDA_ERR_ALIGN
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(bits=3), _lib.QDA_ERR_UNSUPPORTED),
+    (dict(bits=2), _lib.QDA_ERR_UNSUPPORTED),
+    (dict(GS=48), _lib.QDA_ERR_UNSUPPORTED),
+    (dict(GS=16), _lib.QDA_ERR_UNSUPPORTED),
+    (dict(D=96, GS=32), _lib.QDA_ERR_UNSUPPORTED),
+    (dict(D=1024, GS=64), _lib.QDA_ERR_UNSUPPORTED),
+    (dict(D=64, GS=128), _lib.QDA_ERR_UNSUPPORTED),
+    (dict(H=6, Hkv=4), _lib.QDA_ERR_INVALID),
+    (dict(N=(0,)), _lib.QDA_ERR_INVALID),
+    (dict(B=2, N=(5, -1)), _lib.QDA_ERR_INVALID),
+    (dict(B=0, N=(1,)), _lib.QDA_ERR_INVALID),
+    (dict(H=0), _lib.QDA_ERR_INVALID),
+    (dict(Hkv=0), _lib.QDA_ERR_INVALID),
+    (dict(B=_lib.QDA_MAX_B + 1, N=(4,) * (_lib.QDA_MAX_B + 1)), _lib.QDA_ERR_UNSUPPORTED),
+    (dict(H=130, Hkv=2), _lib.QDA_ERR_UNSUPPORTED),
+    (dict(dtype=0), _lib.QDA_ERR_INVALID),
+    (dict(dtype=3), _lib.QDA_ERR_INVALID),            # fp32 input is not a cache dtype
+    (dict(dtype=1 | (4 << 8)), _lib.QDA_ERR_INVALID),
+    (dict(dtype=1 | (1 << 16)), _lib.QDA_ERR_INVALID),
+])
+def test_argument_errors(L, kw, status):
+    assert call(L, **kw) == status
+
+
+def test_null_lengths_invalid(L):
+    assert L.qdecode_attn(*[FAKE] * 8, 1, 8, 2, None, 256, 64, 4, 1, None) == _lib.QDA_ERR_INVALID
+
+
+def test_quantize_argument_errors(L):
+    q = L.qdecode_quantize
+    assert q(None, 4, 256, 64, 4, 1, FAKE, FAKE, FAKE, None) == _lib.QDA_ERR_INVALID
+    assert q(FAKE, 0, 256, 64, 4, 1, FAKE, FAKE, FAKE, None) == _lib.QDA_ERR_INVALID
+    assert q(FAKE, 4, 256, 64, 3, 1, FAKE, FAKE, FAKE, None) == _lib.QDA_ERR_UNSUPPORTED
+    assert q(FAKE, 4, 256, 48, 4, 1, FAKE, FAKE, FAKE, None) == _lib.QDA_ERR_UNSUPPORTED
+    assert q(FAKE + 4, 4, 256, 64, 4, 1, FAKE, FAKE, FAKE, None) == _lib.QDA_ERR_ALIGN
+    assert q(FAKE, 4, 256, 64, 4, 7, FAKE, FAKE, FAKE, None) == _lib.QDA_ERR_INVALID
+
+
+def test_strerror_covers_codes(L):
+    for s in (0, -1, -2, -3, -4, -5):
+        assert len(L.qdecode_attn_strerror(s)) > 5
+    assert L.qdecode_attn_strerror(-99) == b"unknown status"
+
+
+def plan(L, B, H, Hkv, N, D, GS, bits, sms=152, occ=2):
+    p = _lib.QdaPlan()
+    st = L.qdecode_attn_plan(B, H, Hkv, _lib.int32_array(N), D, GS, bits, sms, occ, ctypes.byref(p))
+    assert st == 0
+    return p.as_dict()
+
+
+def cta_row(T, C, c):
+    if c >= C:
+        return T
+    if c <= 0:
+        return 0
+    return ((T * c) // C) & ~7
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 8, 2, [512], 256, 64, 4),
+    (1, 16, 8, [8192], 256, 32, 8),
+    (1, 16, 8, [32768], 512, 128, 4),
+    (8, 32, 8, [1024, 65536, 3001, 40000, 17, 9999, 1, 65000], 256, 64, 4),
+    (1, 16, 4, [131072], 256, 32, 4),
+    (3, 24, 3, [5, 7, 9], 128, 32, 8),
+])
+def test_plan_properties(L, shape):
+    B, H, Hkv, N, D, GS, bits = shape
+    p = plan(L, *shape)
+    T = Hkv * sum(N)
+    assert p["total_rows"] == T
+    assert p["units"] == B * Hkv
+    assert p["slots"] == p["num_ctas"] + B * Hkv
+    nrep = H // Hkv
+    assert p["heads_per_cta"] * p["head_chunks"] >= nrep
+    assert p["heads_per_cta"] & (p["heads_per_cta"] - 1) == 0
+    C = p["num_ctas"]
+    assert 1 <= C <= 152 * 2
+    assert C == 1 or T // C >= 120          # no range much below the per-CTA row floor
+    bounds = [cta_row(T, C, c) for c in range(C + 1)]
+    assert bounds[0] == 0 and bounds[-1] == T
+    assert all(a <= b for a, b in zip(bounds, bounds[1:]))
+    assert all(b % 8 == 0 for b in bounds[1:-1])
+    assert p["tile_rows"] % 16 == 0 and p["stages"] >= 2
+    assert p["smem_bytes"] <= 227 * 1024
+    hp = p["heads_per_cta"] * p["head_chunks"]
+    assert p["workspace_bytes"] >= p["slots"] * hp * (D + 2) * 4
+    assert plan(L, *shape) == p                    # deterministic
+
+
+def test_force_splits(L):
+    try:
+        assert L.qdecode_attn_debug_force_splits(7) == 0
+        assert plan(L, 1, 8, 2, [512], 256, 64, 4)["num_ctas"] == 7
+        assert L.qdecode_attn_debug_force_splits(-1) == _lib.QDA_ERR_INVALID
+    finally:
+        L.qdecode_attn_debug_force_splits(0)
+    assert plan(L, 1, 8, 2, [512], 256, 64, 4)["num_ctas"] == 8
+
+
+def test_plan_argument_errors(L):
+    p = _lib.QdaPlan()
+    assert L.qdecode_attn_plan(1, 8, 2, _lib.int32_array([4]), 256, 64, 4, 152, 2, None) == _lib.QDA_ERR_INVALID
+    assert L.qdecode_attn_plan(1, 8, 3, _lib.int32_array([4]), 256, 64, 4, 152, 2, ctypes.byref(p)) == -1
+    assert L.qdecode_attn_plan(1, 8, 2, _lib.int32_array([4]), 256, 64, 5, 152, 2, ctypes.byref(p)) == -2
