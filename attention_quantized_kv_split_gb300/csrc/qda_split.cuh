@@ -16,6 +16,10 @@
 
 #include <cuda_fp16.h>
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "qda_internal.h"
 #include "qda_ptx.cuh"
 
@@ -349,10 +353,28 @@ cudaError_t with_split_kernel(int wpl, int lpr, int nh, Fn&& f) {
   return cudaErrorInvalidValue;
 }
 
+// Raises a kernel's dynamic shared-memory limit to the opt-in maximum, once per (kernel, device).
+template <typename K>
+cudaError_t ensure_smem_limit(K kern, size_t smem) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  (void)smem;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const auto key = std::make_pair(reinterpret_cast<const void*>(kern), dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count(key)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e != cudaSuccess) return e;
+  done.insert(key);
+  return cudaSuccess;
+}
+
 template <int BITS, bool F16>
 cudaError_t launch_split(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s) {
   return with_split_kernel<BITS, F16>(wpl, lpr, nh, [&](auto kern) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem_limit(kern, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, QDA_THREADS, smem, s>>>(p);
     return cudaGetLastError();
@@ -362,7 +384,7 @@ cudaError_t launch_split(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid
 template <int BITS, bool F16>
 cudaError_t occupancy_split(int wpl, int lpr, int nh, size_t smem, int* n) {
   return with_split_kernel<BITS, F16>(wpl, lpr, nh, [&](auto kern) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem_limit(kern, smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, QDA_THREADS, smem);
   });

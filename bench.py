@@ -301,6 +301,7 @@ def run_ours(args):
     for k in range(rsteps):
         flush()
         ev0[k].record(stream)
+        ev1[k].record(stream)          # marks the event recorded for torch; the library re-records it in the call
         qda.qdecode_attn_set_split_event(ev1[k])
         call()
         qda.qdecode_attn_set_split_event(None)

@@ -58,7 +58,7 @@ def test_append_into_cache_rows():
     cache = qda.QuantizedKV.empty([10], 1, D, GS, bits, torch.bfloat16)
     for t in (cache.kp, cache.vp):
         t.fill_(-1)
-    x = inputs(3, D, 1)
+    x = inputs(8, D, 1)[5:8].copy()
     cache.quantize_into(0, 0, torch.from_numpy(x).cuda(), torch.from_numpy(x).cuda(), row0=4)
     kp = O.quantize_cache(x, x, GS, bits, dtype)[0]
     got = cache.kp.cpu().numpy().view(np.uint32)
