@@ -52,6 +52,25 @@ def qdecode_attn(q: torch.Tensor, k_packed: torch.Tensor, k_scales: torch.Tensor
     return out
 
 
+def bind_qdecode_attn(q: torch.Tensor, k_packed: torch.Tensor, k_scales: torch.Tensor, k_biases: torch.Tensor,
+                      v_packed: torch.Tensor, v_scales: torch.Tensor, v_biases: torch.Tensor, out: torch.Tensor,
+                      N: Sequence[int], Hkv: int, GS: int, bits: int, stream=None):
+    """qdecode_attn with every argument marshalled once: returns a no-argument callable for repeated calls on
+    the same buffers (decode loops, timing)."""
+    B, H, D = q.shape
+    args = (_ptr(q), _ptr(k_packed), _ptr(k_scales), _ptr(k_biases), _ptr(v_packed), _ptr(v_scales),
+            _ptr(v_biases), _ptr(out), B, H, Hkv, _lib.int32_array(N), D, GS, bits, dtype_code(q.dtype, out.dtype),
+            _stream(stream))
+    fn = lib().qdecode_attn
+
+    def call():
+        st = fn(*args)
+        if st:
+            raise _lib.QdaError(st, "qdecode_attn")
+    call.keepalive = (q, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, out)
+    return call
+
+
 def qdecode_attn_plan(B: int, H: int, Hkv: int, N: Sequence[int], D: int, GS: int, bits: int, num_sms: int = 0,
                       ctas_per_sm: int = 0) -> dict:
     plan = QdaPlan()
@@ -141,6 +160,12 @@ class QuantizedKV:
 
     def nbytes(self) -> int:
         return sum(t.numel() * t.element_size() for t in (self.kp, self.ks, self.kb, self.vp, self.vs, self.vb))
+
+
+def bind_decode_attention(q: torch.Tensor, cache: QuantizedKV, out: torch.Tensor, stream=None):
+    """Pre-marshalled decode_attention over a QuantizedKV (see bind_qdecode_attn)."""
+    return bind_qdecode_attn(q, cache.kp, cache.ks, cache.kb, cache.vp, cache.vs, cache.vb, out, cache.N, cache.Hkv,
+                             cache.GS, cache.bits, stream)
 
 
 def decode_attention(q: torch.Tensor, cache: QuantizedKV, out_dtype: Optional[torch.dtype] = None,

@@ -24,7 +24,8 @@ struct QdaParams {
   float2* part_ml;            // [slots, heads_pad] (running max in log2 units, sum of 2^(s - max))
   unsigned int* err;          // device error word
   long long total_rows;       // T = Hkv * sum(N)
-  int B, H, Hkv, D, GS, NG, W, nrep, heads_pad, num_ctas, tile_rows, stages;
+  int B, H, Hkv, D, GS, NG, W, nrep, heads_pad, head_chunks, num_ctas, tile_rows, stages;
+  int f16;                    // q / scales / biases are fp16 (else bf16)
   float qscale;               // log2(e) / sqrt(D): scores come out in log2 units
   int seq_off[QDA_MAX_B + 1]; // seq_off[b] = N[0] + ... + N[b-1]
 };
@@ -67,16 +68,27 @@ __host__ __device__ inline QdaSmemLayout qda_smem_layout(int tile_rows, int stag
   return L;
 }
 
-// Launchers (one translation unit per bits x input dtype). They return cudaSuccess or the launch error.
-// blk: the (bits, words-per-lane, lanes-per-row, heads-per-CTA) variant; grid = (num_ctas, head_chunks).
-cudaError_t qda_launch_split_b4_bf16(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s);
-cudaError_t qda_launch_split_b4_fp16(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s);
-cudaError_t qda_launch_split_b8_bf16(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s);
-cudaError_t qda_launch_split_b8_fp16(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s);
-cudaError_t qda_occupancy_split_b4_bf16(int wpl, int lpr, int nh, size_t smem, int* ctas_per_sm);
-cudaError_t qda_occupancy_split_b4_fp16(int wpl, int lpr, int nh, size_t smem, int* ctas_per_sm);
-cudaError_t qda_occupancy_split_b8_bf16(int wpl, int lpr, int nh, size_t smem, int* ctas_per_sm);
-cudaError_t qda_occupancy_split_b8_fp16(int wpl, int lpr, int nh, size_t smem, int* ctas_per_sm);
+// Lean split kernel: floats of per-warp scratch (K coefficients (A, A, B, B) and V coefficients A_v, B_v per
+// (row, group), p * A_v pairs per (row, group, head), per-head sums of p * B_v per group).
+__host__ __device__ inline int split2_scratch_floats(int R, int NG, int NH) {
+  return R * NG * (4 + 2 + 2 * NH) + NH * NG;
+}
+
+// Launchers of the split kernels, one translation unit per (kernel, bits[, exact]). They return cudaSuccess or the
+// launch error. General kernel: (words per lane, lanes per row, heads per CTA); lean kernel: (D, heads per CTA,
+// groups per row, exact V codes).
+cudaError_t qda_launch_split1_b4(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s);
+cudaError_t qda_launch_split1_b8(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s);
+cudaError_t qda_occupancy_split1_b4(int wpl, int lpr, int nh, size_t smem, int* ctas_per_sm);
+cudaError_t qda_occupancy_split1_b8(int wpl, int lpr, int nh, size_t smem, int* ctas_per_sm);
+cudaError_t qda_launch_split2_b4_x0(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem, cudaStream_t s);
+cudaError_t qda_launch_split2_b4_x1(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem, cudaStream_t s);
+cudaError_t qda_launch_split2_b8_x0(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem, cudaStream_t s);
+cudaError_t qda_launch_split2_b8_x1(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem, cudaStream_t s);
+cudaError_t qda_occupancy_split2_b4_x0(int D, int nh, int ng, size_t smem, int* ctas_per_sm);
+cudaError_t qda_occupancy_split2_b4_x1(int D, int nh, int ng, size_t smem, int* ctas_per_sm);
+cudaError_t qda_occupancy_split2_b8_x0(int D, int nh, int ng, size_t smem, int* ctas_per_sm);
+cudaError_t qda_occupancy_split2_b8_x1(int D, int nh, int ng, size_t smem, int* ctas_per_sm);
 
 cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool pdl, cudaStream_t s);
 

@@ -33,15 +33,21 @@ __device__ __forceinline__ void store4(void* out, size_t idx, float4 v) {
 }
 
 // out[b, h, :] = sum_s o_s 2^(m_s - M) / sum_s l_s 2^(m_s - M) over the partial slots of (b, KV head of h)
-// (mlx-bun fused-decode-kernel.ts, MERGE_SOURCE), in log2 units. One CTA per (b, h); the slots are dealt to
-// 256 / (D/4) thread groups round-robin and the groups are summed in a fixed order: deterministic, no atomics.
+// (mlx-bun fused-decode-kernel.ts, MERGE_SOURCE), in log2 units. One CTA per (b, h). The slot weights are staged
+// in shared memory once; the o rows are dealt to 256 / (D/4) thread groups round-robin and every sum runs in a
+// fixed order, so the result is deterministic without atomics.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeMaxSlots = 4096;
+
 template <int OUT>
-__global__ void __launch_bounds__(256) qda_merge_kernel(const __grid_constant__ QdaParams p, void* __restrict__ out) {
-  pdl_wait();
+__global__ void __launch_bounds__(kMergeThreads) qda_merge_kernel(const __grid_constant__ QdaParams p,
+                                                                  void* __restrict__ out) {
+  __shared__ float s_w[kMergeMaxSlots];   // slot max, then slot weight 2^(m_s - M) (0 for an empty range)
+  __shared__ float s_l[kMergeMaxSlots];   // slot sum, then weighted
+  __shared__ float4 red[kMergeThreads];
+  __shared__ float redf[kMergeThreads];
+  const int tid = threadIdx.x;
   const int D = p.D;
-  const int tpr = D >> 2;
-  const int groups = blockDim.x / tpr;
-  const int grp = threadIdx.x / tpr, t = threadIdx.x - grp * tpr;
   const int bh = blockIdx.x;
   const int b = bh / p.H, h = bh - b * p.H;
   const int kvh = h / p.nrep, j = h - kvh * p.nrep;
@@ -49,46 +55,72 @@ __global__ void __launch_bounds__(256) qda_merge_kernel(const __grid_constant__ 
   const long long n = p.seq_off[b + 1] - p.seq_off[b];
   const long long us = (long long)p.Hkv * p.seq_off[b] + (long long)kvh * n;
   const long long T = p.total_rows;
-  const int cf = qda_cta_of(T, p.num_ctas, us);
-  const int cl = qda_cta_of(T, p.num_ctas, us + n - 1);
+  const int C = p.num_ctas;
+  const int cf = qda_cta_of(T, C, us);
+  const int ns = qda_cta_of(T, C, us + n - 1) - cf + 1;
 
-  // CTAs with an empty row range (possible only when ranges are shorter than 8 rows) wrote no slot
-  float M = -INFINITY;
-  for (int c = cf; c <= cl; ++c) {
-    if (qda_cta_row(T, p.num_ctas, c) == qda_cta_row(T, p.num_ctas, c + 1)) continue;
-    M = fmaxf(M, p.part_ml[(size_t)(c + unit) * p.heads_pad + j].x);
+  pdl_wait();   // the split kernel's partials are complete and visible from here on
+
+  // slot statistics; CTAs with an empty row range (ranges shorter than 8 rows) wrote no slot
+  float mx = -INFINITY;
+  for (int k = tid; k < ns; k += kMergeThreads) {
+    const int c = cf + k;
+    float m = -INFINITY, l = 0.f;
+    if (qda_cta_row(T, C, c) != qda_cta_row(T, C, c + 1)) {
+      const float2 ml = p.part_ml[(size_t)(c + unit) * p.heads_pad + j];
+      m = ml.x;
+      l = ml.y;
+    }
+    s_w[k] = m;
+    s_l[k] = l;
+    mx = fmaxf(mx, m);
   }
-
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  redf[tid] = mx;
+  __syncthreads();
+  for (int w = kMergeThreads / 2; w > 0; w >>= 1) {
+    if (tid < w) redf[tid] = fmaxf(redf[tid], redf[tid + w]);
+    __syncthreads();
+  }
+  const float M = redf[0];
+  __syncthreads();
   float den = 0.f;
-  for (int c = cf + grp; c <= cl; c += groups) {
-    if (qda_cta_row(T, p.num_ctas, c) == qda_cta_row(T, p.num_ctas, c + 1)) continue;
-    const size_t hp = (size_t)(c + unit) * p.heads_pad + j;
-    const float2 ml = p.part_ml[hp];
-    const float wt = ex2m(ml.x - M);
-    den = fmaf(ml.y, wt, den);
+  for (int k = tid; k < ns; k += kMergeThreads) {
+    const float wt = ex2m(s_w[k] - M);   // 2^-inf = 0 for empty slots
+    s_w[k] = wt;
+    den = fmaf(s_l[k], wt, den);
+  }
+  redf[tid] = den;
+  __syncthreads();
+  for (int w = kMergeThreads / 2; w > 0; w >>= 1) {
+    if (tid < w) redf[tid] += redf[tid + w];
+    __syncthreads();
+  }
+  const float inv = 1.0f / redf[0];
+
+  const int tpr = D >> 2;
+  const int groups = kMergeThreads / tpr;
+  const int grp = tid / tpr, t = tid - grp * tpr;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = grp; k < ns; k += groups) {
+    const float wt = s_w[k];
+    if (wt == 0.f) continue;
+    const size_t hp = (size_t)(cf + k + unit) * p.heads_pad + j;
     const float4 v = reinterpret_cast<const float4*>(p.part_o + hp * D)[t];
     acc.x = fmaf(v.x, wt, acc.x);
     acc.y = fmaf(v.y, wt, acc.y);
     acc.z = fmaf(v.z, wt, acc.z);
     acc.w = fmaf(v.w, wt, acc.w);
   }
-  __shared__ float4 red[256];
-  __shared__ float dred[256];
-  red[threadIdx.x] = acc;
-  if (t == 0) dred[grp] = den;
+  red[tid] = acc;
   __syncthreads();
   if (grp != 0) return;
-  float dt = dred[0];
   for (int g = 1; g < groups; ++g) {
     const float4 v = red[g * tpr + t];
     acc.x += v.x;
     acc.y += v.y;
     acc.z += v.z;
     acc.w += v.w;
-    dt += dred[g];
   }
-  const float inv = 1.0f / dt;
   acc.x *= inv;
   acc.y *= inv;
   acc.z *= inv;
@@ -206,7 +238,7 @@ cudaError_t launch_quant(const float* x, long long rows, int D, int GS, uint32_t
 cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.B * p.H));
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(qda::kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -106,4 +106,9 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t u16) {
   }
 }
 
+// bf16 or fp16 bits -> float, dtype chosen at run time (a warp-uniform select)
+__device__ __forceinline__ float half_bits_to_float_rt(uint32_t u16, bool f16) {
+  return f16 ? fp16_bits_to_float(u16) : bf16_bits_to_float(u16);
+}
+
 }  // namespace qda

@@ -80,9 +80,52 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   }
 }
 
+// The producer lane: walks the CTA's chunks and fills the shared-memory ring. Per chunk: the K and V codes of its
+// rows and the 8-row aligned cover of its scales/biases (clipped to the arrays' end; a ragged last < 16 bytes go
+// by plain loads, published by the arrive), all completing on full[stage]. Waits for the consumers to free a
+// stage (empty[stage]) before reusing it; before returning it waits until every copy it issued has landed.
+__device__ __forceinline__ void produce_range(const QdaParams& p, ChunkWalker walk, unsigned char* smem,
+                                              const QdaSmemLayout& L, uint64_t* full, uint64_t* empty,
+                                              volatile int* abort_flag, long long T) {
+  const int STAGES = p.stages, NG = p.NG, W = p.W;
+  const uint64_t pol = policy_evict_first();
+  const uint32_t RB = W * 4, SB = NG * 2;
+  long long c0, c1, t0;
+  int i = 0;
+  while (walk.next(p, c0, c1, t0)) {
+    const int s = i % STAGES;
+    if (i >= STAGES && !mbar_wait_bounded(&empty[s], ((i / STAGES) - 1) & 1, abort_flag, p.err, 1u)) break;
+    unsigned char* st = smem + L.stage0 + (size_t)s * L.stage_bytes;
+    const uint32_t cbytes = (uint32_t)(c1 - c0) * RB;
+    const size_t coff = (size_t)(c0 - t0) * RB;
+    const long long s0 = c0 & ~7LL;
+    const long long s1 = min((c1 + 7) & ~7LL, T);
+    const uint32_t sbytes = (uint32_t)(s1 - s0) * SB;
+    const uint32_t s16 = sbytes & ~15u;
+    const size_t soff = (size_t)(s0 - t0) * SB;
+    const uint16_t* srcs[4] = {p.ks, p.kb, p.vs, p.vb};
+    if (s16 != sbytes) {
+      for (int a = 0; a < 4; ++a) {
+        const uint16_t* src = srcs[a] + s0 * NG + s16 / 2;
+        uint16_t* dst = reinterpret_cast<uint16_t*>(st + 2 * L.codes_bytes + a * L.sc_bytes + soff + s16);
+        for (uint32_t k = 0; k < (sbytes - s16) / 2; ++k) dst[k] = src[k];
+      }
+    }
+    mbar_arrive_expect_tx(&full[s], 2 * cbytes + 4 * s16);
+    bulk_g2s(st + coff, p.kp + c0 * W, cbytes, &full[s], pol);
+    bulk_g2s(st + L.codes_bytes + coff, p.vp + c0 * W, cbytes, &full[s], pol);
+    if (s16) {
+      for (int a = 0; a < 4; ++a)
+        bulk_g2s(st + 2 * L.codes_bytes + a * L.sc_bytes + soff, srcs[a] + s0 * NG, s16, &full[s], pol);
+    }
+    ++i;
+  }
+  for (int j = (i > STAGES ? i - STAGES : 0); j < i; ++j) mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1, p.err);
+}
+
 // BITS: 4 or 8. WPL: packed words per lane per row. LPR: lanes per row (RPS = 32/LPR rows per warp step).
-// NH: query heads per CTA. F16: fp16 (else bf16) q / scales / biases. D = LPR * WPL * 32 / BITS.
-template <int BITS, int WPL, int LPR, int NH, bool F16>
+// NH: query heads per CTA. D = LPR * WPL * 32 / BITS.
+template <int BITS, int WPL, int LPR, int NH>
 __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_constant__ QdaParams p) {
   constexpr int PER = 32 / BITS;          // codes per word
   constexpr int E = WPL * PER;            // elements per lane per row
@@ -102,8 +145,10 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
   float* comb_m = comb_o + NW * NH * D;
   float* comb_l = comb_m + NW * NH;
 
+  const bool f16 = p.f16 != 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cta = blockIdx.x, hc = blockIdx.y;
+  // head chunks of one row range are adjacent blocks, so a second chunk re-reads rows while they are in L2
+  const int cta = blockIdx.x / p.head_chunks, hc = blockIdx.x - cta * p.head_chunks;
   const long long T = p.total_rows;
   const long long r0 = qda_cta_row(T, p.num_ctas, cta);
   const long long r1 = qda_cta_row(T, p.num_ctas, cta + 1);
@@ -125,41 +170,7 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
   long long c0, c1, t0;
 
   if (warp == NW) {
-    // ---------------------------------------------------------------- producer: one lane issues every copy
-    if (lane != 0) return;
-    const uint64_t pol = policy_evict_first();
-    const uint32_t RB = W * 4, SB = NG * 2;
-    int i = 0;
-    while (walk.next(p, c0, c1, t0)) {
-      const int s = i % STAGES;
-      if (i >= STAGES && !mbar_wait_bounded(&empty[s], ((i / STAGES) - 1) & 1, abort_flag, p.err, 1u)) break;
-      unsigned char* st = smem + L.stage0 + (size_t)s * L.stage_bytes;
-      const uint32_t cbytes = (uint32_t)(c1 - c0) * RB;
-      const size_t coff = (size_t)(c0 - t0) * RB;
-      // scales/biases: the 8-row aligned cover of [c0, c1), clipped to the end of the arrays
-      const long long s0 = c0 & ~7LL;
-      const long long s1 = min((c1 + 7) & ~7LL, T);
-      const uint32_t sbytes = (uint32_t)(s1 - s0) * SB;
-      const uint32_t s16 = sbytes & ~15u;
-      const size_t soff = (size_t)(s0 - t0) * SB;
-      const uint16_t* srcs[4] = {p.ks, p.kb, p.vs, p.vb};
-      if (s16 != sbytes) {  // the last (< 16) bytes of the arrays: plain loads, published by the arrive below
-        for (int a = 0; a < 4; ++a) {
-          const uint16_t* src = srcs[a] + s0 * NG + s16 / 2;
-          uint16_t* dst = reinterpret_cast<uint16_t*>(st + 2 * L.codes_bytes + a * L.sc_bytes + soff + s16);
-          for (uint32_t k = 0; k < (sbytes - s16) / 2; ++k) dst[k] = src[k];
-        }
-      }
-      mbar_arrive_expect_tx(&full[s], 2 * cbytes + 4 * s16);
-      bulk_g2s(st + coff, p.kp + c0 * W, cbytes, &full[s], pol);
-      bulk_g2s(st + L.codes_bytes + coff, p.vp + c0 * W, cbytes, &full[s], pol);
-      if (s16) {
-        for (int a = 0; a < 4; ++a)
-          bulk_g2s(st + 2 * L.codes_bytes + a * L.sc_bytes + soff, srcs[a] + s0 * NG, s16, &full[s], pol);
-      }
-      ++i;
-    }
-    for (int j = (i > STAGES ? i - STAGES : 0); j < i; ++j) mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1, p.err);
+    if (lane == 0) produce_range(p, walk, smem, L, full, empty, abort_flag, T);
     return;
   }
 
@@ -181,7 +192,7 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
                                ((size_t)walk.b * p.H + (size_t)walk.kvh * p.nrep + j) * D + lir * E;
 #pragma unroll
           for (int e = 0; e < E; ++e) {
-            qv[h][e] = half_bits_to_float<F16>(qp[e]) * p.qscale;
+            qv[h][e] = half_bits_to_float_rt(qp[e], f16) * p.qscale;
             acc += qv[h][e];
           }
         } else {
@@ -219,8 +230,8 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
           for (int k = 0; k < PER; ++k)
             cf[w * PER + k] = __uint_as_float(0x4B000000u | ((word >> (BITS * k)) & MASK)) - 8388608.0f;
         }
-        const float ksc = half_bits_to_float<F16>(sKS[lr * NG + g]);
-        const float kbi = half_bits_to_float<F16>(sKB[lr * NG + g]);
+        const float ksc = half_bits_to_float_rt(sKS[lr * NG + g], f16);
+        const float kbi = half_bits_to_float_rt(sKB[lr * NG + g], f16);
         float sc[NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
@@ -261,8 +272,8 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
           for (int k = 0; k < PER; ++k)
             cf[w * PER + k] = __uint_as_float(0x4B000000u | ((word >> (BITS * k)) & MASK)) - 8388608.0f;
         }
-        const float vsc = half_bits_to_float<F16>(sVS[lr * NG + g]);
-        const float vbi = half_bits_to_float<F16>(sVB[lr * NG + g]);
+        const float vsc = half_bits_to_float_rt(sVS[lr * NG + g], f16);
+        const float vbi = half_bits_to_float_rt(sVB[lr * NG + g], f16);
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
           const float ps = pr[h] * vsc, pb = pr[h] * vbi;
@@ -326,15 +337,15 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
 }
 
 // Calls f(kernel) with the instantiation for (wpl, lpr, nh); returns cudaErrorInvalidValue for an unbuilt one.
-template <int BITS, bool F16, typename Fn>
+template <int BITS, typename Fn>
 cudaError_t with_split_kernel(int wpl, int lpr, int nh, Fn&& f) {
 #define QDA_NH_CASES(WPL_, LPR_)                                                        \
   switch (nh) {                                                                         \
-    case 1: return f(qda_split_kernel<BITS, WPL_, LPR_, 1, F16>);                       \
-    case 2: return f(qda_split_kernel<BITS, WPL_, LPR_, 2, F16>);                       \
-    case 4: return f(qda_split_kernel<BITS, WPL_, LPR_, 4, F16>);                       \
+    case 1: return f(qda_split_kernel<BITS, WPL_, LPR_, 1>);                       \
+    case 2: return f(qda_split_kernel<BITS, WPL_, LPR_, 2>);                       \
+    case 4: return f(qda_split_kernel<BITS, WPL_, LPR_, 4>);                       \
     case 8:                                                                             \
-      if constexpr (WPL_ * (32 / BITS) * 8 <= 64) return f(qda_split_kernel<BITS, WPL_, LPR_, 8, F16>); \
+      if constexpr (WPL_ * (32 / BITS) * 8 <= 64) return f(qda_split_kernel<BITS, WPL_, LPR_, 8>); \
       else return cudaErrorInvalidValue;                                                \
     default: return cudaErrorInvalidValue;                                              \
   }
@@ -371,9 +382,9 @@ cudaError_t ensure_smem_limit(K kern, size_t smem) {
   return cudaSuccess;
 }
 
-template <int BITS, bool F16>
+template <int BITS>
 cudaError_t launch_split(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s) {
-  return with_split_kernel<BITS, F16>(wpl, lpr, nh, [&](auto kern) -> cudaError_t {
+  return with_split_kernel<BITS>(wpl, lpr, nh, [&](auto kern) -> cudaError_t {
     cudaError_t e = ensure_smem_limit(kern, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, QDA_THREADS, smem, s>>>(p);
@@ -381,9 +392,9 @@ cudaError_t launch_split(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid
   });
 }
 
-template <int BITS, bool F16>
+template <int BITS>
 cudaError_t occupancy_split(int wpl, int lpr, int nh, size_t smem, int* n) {
-  return with_split_kernel<BITS, F16>(wpl, lpr, nh, [&](auto kern) -> cudaError_t {
+  return with_split_kernel<BITS>(wpl, lpr, nh, [&](auto kern) -> cudaError_t {
     cudaError_t e = ensure_smem_limit(kern, smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, QDA_THREADS, smem);

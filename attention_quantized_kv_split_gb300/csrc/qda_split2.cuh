@@ -1,0 +1,484 @@
+// Split kernel, arithmetic-lean variant: D = 256 with 2 or 4 query heads per CTA, D = 512 with 2 (sm_103a).
+//
+// Same data path as qda_split_kernel (one contiguous row range per CTA, producer warp + bulk copies into a
+// shared-memory ring, one partial per (segment, query head)), but the consumer warps are organised around the
+// instruction count per cache row, which bounds this path once the bytes stream at HBM speed:
+//   * codes become floats with one byte permute each: 4-bit codes as 0.5 + c/256 (K, and V for 16-bit outputs),
+//     8-bit codes as 1 + c/32768 (K for 16-bit outputs), or exactly as c (2^23 + c minus 2^23) where an fp32
+//     output needs it; the constant offset is folded into per-row coefficients A, B with
+//     s*c + b = A*f + B, computed once per (row, group) by the warp before its rows are used;
+//   * every dot product and every V update is a packed two-lane FMA (f32x2);
+//   * K rows are read by 16 lanes (16 codes each) and the per-row sums are formed by a transposed butterfly,
+//     so each lane ends with whole scores for fixed (rows, head) instead of every lane reducing every score;
+//   * the online softmax advances once per block of R rows per warp (one max, one rescale of o when it moves);
+//   * the lane that owns a score also forms p * A_v for every group of that row (the V coefficient of the
+//     mlx-bun SCORE_ROW factoring, applied to V) and keeps the sum of p * B_v, so the V lanes only load them.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "qda_split.cuh"
+
+namespace qda {
+
+// ----------------------------------------------------------------------------- code -> float conversions
+
+// 4-bit, one word (8 codes, code k at bits 4k..4k+3) -> 4 pairs (code 2j, code 2j+1).
+template <bool EXACT>
+__device__ __forceinline__ void unpack4(uint32_t w, float2 (&f)[4]) {
+  const uint32_t lo = w & 0x0F0F0F0Fu;          // codes 0, 2, 4, 6 in bytes 0..3
+  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;   // codes 1, 3, 5, 7
+  if constexpr (EXACT) {
+    // bytes [code, 0, 0, 0x4B] = 2^23 + code
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t sel = 0x7650u | (uint32_t)j;
+      f[j] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, sel)),
+                                    __uint_as_float(__byte_perm(hi, 0x4B000000u, sel))),
+                        make_float2(-8388608.0f, -8388608.0f));
+    }
+  } else {
+    // bytes [0, 0, code, 0x3F] = 0.5 + code / 256
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t sel = 0x7054u | ((uint32_t)j << 8);
+      f[j] = make_float2(__uint_as_float(__byte_perm(lo, 0x3F000000u, sel)),
+                         __uint_as_float(__byte_perm(hi, 0x3F000000u, sel)));
+    }
+  }
+}
+
+// 8-bit, one word (4 codes, code k in byte k) -> 2 pairs.
+template <bool EXACT>
+__device__ __forceinline__ void unpack8(uint32_t w, float2 (&f)[2]) {
+  if constexpr (EXACT) {
+    f[0] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7650u)),
+                                  __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7651u))),
+                      make_float2(-8388608.0f, -8388608.0f));
+    f[1] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7652u)),
+                                  __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7653u))),
+                      make_float2(-8388608.0f, -8388608.0f));
+  } else {
+    // bytes [0, code, 0x80, 0x3F] = 1 + code / 32768
+    f[0] = make_float2(__uint_as_float(__byte_perm(w, 0x3F800000u, 0x7604u)),
+                       __uint_as_float(__byte_perm(w, 0x3F800000u, 0x7614u)));
+    f[1] = make_float2(__uint_as_float(__byte_perm(w, 0x3F800000u, 0x7624u)),
+                       __uint_as_float(__byte_perm(w, 0x3F800000u, 0x7634u)));
+  }
+}
+
+// A word array -> NW2 * (32/BITS) / 2 pairs.
+template <int BITS, bool EXACT, int NWORDS>
+__device__ __forceinline__ void unpack_words(const uint32_t (&w)[NWORDS], float2 (&f)[NWORDS * 16 / BITS]) {
+#pragma unroll
+  for (int k = 0; k < NWORDS; ++k) {
+    if constexpr (BITS == 4) {
+      float2 t[4];
+      unpack4<EXACT>(w[k], t);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) f[4 * k + j] = t[j];
+    } else {
+      float2 t[2];
+      unpack8<EXACT>(w[k], t);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) f[2 * k + j] = t[j];
+    }
+  }
+}
+
+// s * c + b = A * f + B for the encoding above.
+template <int BITS, bool EXACT>
+__device__ __forceinline__ float2 coeffs(float s, float b) {
+  if constexpr (EXACT) {
+    return make_float2(s, b);
+  } else if constexpr (BITS == 4) {
+    return make_float2(256.0f * s, fmaf(-128.0f, s, b));
+  } else {
+    return make_float2(32768.0f * s, fmaf(-32768.0f, s, b));
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void load_words(const uint32_t* src, uint32_t (&w)[N]) {
+  if constexpr (N == 1) {
+    w[0] = src[0];
+  } else if constexpr (N == 2) {
+    const uint2 t = *reinterpret_cast<const uint2*>(src);
+    w[0] = t.x;
+    w[1] = t.y;
+  } else {
+#pragma unroll
+    for (int k = 0; k < N; k += 4) {
+      const uint4 t = *reinterpret_cast<const uint4*>(src + k);
+      w[k] = t.x;
+      w[k + 1] = t.y;
+      w[k + 2] = t.z;
+      w[k + 3] = t.w;
+    }
+  }
+}
+
+// Geometry of the lean variant, shared by the kernel and the host.
+template <int BITS, int D, int NH>
+struct Split2Geom {
+  static constexpr int EK = 16;                 // K codes per lane per row
+  static constexpr int LK = D / EK;             // lanes per K row (16 or 32)
+  static constexpr int RPS = 32 / LK;           // K rows per warp step
+  static constexpr int R = NH == 4 ? 8 : 16;  // rows per warp block (fewer live scores with 4 heads)
+  static constexpr int S = R / RPS;             // K steps per block
+  static constexpr int NV = NH * S;             // partial scores per lane before the reduction
+  static constexpr int NVL = NV / LK;           // scores per lane after it
+  static constexpr int EV = D / 32;             // V codes per lane per row
+  static constexpr int KW = EK * BITS / 32;     // K words per lane per row
+  static constexpr int VW = EV * BITS / 32;     // V words per lane per row
+  static constexpr int W = D * BITS / 32;       // words per row
+  static constexpr int TILE = R * QDA_NW;       // rows per pipeline stage
+  static_assert(NVL >= 1, "reduction must end with at least one score per lane");
+};
+
+template <int BITS, int D, int NH, int NG, bool EXACT>
+__global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid_constant__ QdaParams p) {
+  using G = Split2Geom<BITS, D, NH>;
+  constexpr int EK = G::EK, LK = G::LK, RPS = G::RPS, R = G::R, S = G::S, NV = G::NV, NVL = G::NVL;
+  constexpr int EV = G::EV, KW = G::KW, VW = G::VW, W = G::W;
+  constexpr int NW = QDA_NW;
+  constexpr bool EXACT_K = EXACT && BITS == 8;   // 4-bit K scores are accurate enough in the cheap form
+  constexpr int LOG_NH = NH == 4 ? 2 : 1;
+  constexpr int LOG_LK = LK == 32 ? 5 : 4;
+
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int TILE = p.tile_rows, STAGES = p.stages;
+  const bool f16 = p.f16 != 0;
+  const QdaSmemLayout L = qda_smem_layout(TILE, STAGES, W, NG, NH, D);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + STAGES;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
+  float* scratch_all = reinterpret_cast<float*>(smem + L.comb);   // per-warp scratch, reused as combine area
+  float* comb_o = scratch_all;
+  float* comb_m = comb_o + NW * NH * D;
+  float* comb_l = comb_m + NW * NH;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // head chunks of one row range are adjacent blocks, so a second chunk re-reads rows while they are in L2
+  const int cta = blockIdx.x / p.head_chunks, hc = blockIdx.x - cta * p.head_chunks;
+  const long long T = p.total_rows;
+  const long long r0 = qda_cta_row(T, p.num_ctas, cta);
+  const long long r1 = qda_cta_row(T, p.num_ctas, cta + 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NW);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  if (r0 >= r1) return;
+
+  ChunkWalker walk;
+  walk.init(p, r0, r1);
+  long long c0, c1, t0;
+
+  if (warp == NW) {
+    if (lane == 0) produce_range(p, walk, smem, L, full, empty, abort_flag, T);
+    return;
+  }
+
+  // ------------------------------------------------------------------------------ consumer warp state
+  const int sw_floats = split2_scratch_floats(R, NG, NH);
+  float* sAB = scratch_all + warp * sw_floats;          // [R][NG] float4 (A, A, B, B) of K
+  float* sAV = sAB + R * NG * 4;                        // [R][NG] A_v
+  float* sBV = sAV + R * NG;                            // [R][NG] B_v
+  float* sPS = sBV + R * NG;                            // [R][NG][NH] float2 (p A_v, p A_v)
+  float* sPB = sPS + R * NG * NH * 2;                   // [NH][NG]
+
+  const int klane = lane & (LK - 1);                    // K slice: codes [klane*EK, klane*EK + EK)
+  const int khalf = lane / LK;                          // which row of a K step
+  const int gk = (klane * EK) / p.GS;
+  const int gv = (lane * EV) / p.GS;                    // V slice: codes [lane*EV, lane*EV + EV)
+
+  // the head and rows this lane owns after the reduction
+  int my_h = 0;
+#pragma unroll
+  for (int k = 0; k < LOG_NH; ++k) my_h += ((lane >> k) & 1) * (NH >> (k + 1));
+  int my_s[NVL];
+#pragma unroll
+  for (int i = 0; i < NVL; ++i) {
+    int s = i;
+#pragma unroll
+    for (int k = LOG_NH; k < LOG_LK; ++k) s += ((lane >> k) & 1) * (NV >> (k + 1));
+    my_s[i] = s;  // index within the head's S steps (index - h * S)
+  }
+  int head_lane[NH];   // a lane that owns head h
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    int l = 0;
+#pragma unroll
+    for (int k = 0; k < LOG_NH; ++k) l |= ((h >> (LOG_NH - 1 - k)) & 1) << k;
+    head_lane[h] = l;
+  }
+
+  float2 qk[NH][EK / 2];    // q slice for K, pre-scaled to log2 units
+  float qs[NH];             // its sum (bias term)
+  float2 o[NH][EV / 2];     // V accumulators
+  float m_run = -INFINITY;  // running max of my head (equal across the lanes owning it)
+  float l_run = 0.f;        // sum of 2^(s - m_run) over my rows
+  float pb[NG];             // sum of p * B_v per group, my head
+  int cur_unit = -1;
+  int i_chunk = 0;
+
+  while (walk.next(p, c0, c1, t0)) {
+    if (walk.unit != cur_unit) {
+      cur_unit = walk.unit;
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const int j = hc * NH + h;
+        float acc = 0.f;
+        if (j < p.nrep) {
+          const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
+                               ((size_t)walk.b * p.H + (size_t)walk.kvh * p.nrep + j) * D + klane * EK;
+          const uint4 a = reinterpret_cast<const uint4*>(qp)[0];
+          const uint4 b = reinterpret_cast<const uint4*>(qp)[1];
+          const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float x = half_bits_to_float_rt(u[k] & 0xFFFFu, f16) * p.qscale;
+            const float y = half_bits_to_float_rt(u[k] >> 16, f16) * p.qscale;
+            qk[h][k] = make_float2(x, y);
+            acc += x + y;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < EK / 2; ++k) qk[h][k] = make_float2(0.f, 0.f);
+        }
+        qs[h] = acc;
+#pragma unroll
+        for (int k = 0; k < EV / 2; ++k) o[h][k] = make_float2(0.f, 0.f);
+      }
+      m_run = -INFINITY;
+      l_run = 0.f;
+#pragma unroll
+      for (int g = 0; g < NG; ++g) pb[g] = 0.f;
+    }
+
+    const int stage = i_chunk % STAGES;
+    const bool ok = mbar_wait_bounded(&full[stage], (i_chunk / STAGES) & 1, abort_flag, p.err, 1u);
+    const long long b0 = c0 + (long long)warp * R;          // this warp's block of the chunk
+    const int rows_valid = ok ? (int)max(0LL, min((long long)R, c1 - b0)) : 0;
+    if (rows_valid > 0) {
+      const unsigned char* st = smem + L.stage0 + (size_t)stage * L.stage_bytes;
+      const int lr0 = (int)(b0 - t0);                       // block's first row within the stage
+      const uint32_t* sK = reinterpret_cast<const uint32_t*>(st) + (size_t)lr0 * W;
+      const uint32_t* sV = reinterpret_cast<const uint32_t*>(st + L.codes_bytes) + (size_t)lr0 * W;
+      const uint16_t* sKS = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes) + lr0 * NG;
+      const uint16_t* sKB = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes + L.sc_bytes) + lr0 * NG;
+      const uint16_t* sVS = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes + 2 * L.sc_bytes) + lr0 * NG;
+      const uint16_t* sVB = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes + 3 * L.sc_bytes) + lr0 * NG;
+
+      // ---- phase 0: per-(row, group) coefficients of K and V
+      for (int idx = lane; idx < rows_valid * NG; idx += 32) {
+        const float2 ak = coeffs<BITS, EXACT_K>(half_bits_to_float_rt(sKS[idx], f16), half_bits_to_float_rt(sKB[idx], f16));
+        const float2 av = coeffs<BITS, EXACT>(half_bits_to_float_rt(sVS[idx], f16), half_bits_to_float_rt(sVB[idx], f16));
+        reinterpret_cast<float4*>(sAB)[idx] = make_float4(ak.x, ak.x, ak.y, ak.y);
+        sAV[idx] = av.x;
+        sBV[idx] = av.y;
+      }
+      __syncwarp();
+
+      // ---- phase 1: K partial dots, NH heads x S steps per lane
+      float v[NV];
+#pragma unroll
+      for (int s = 0; s < S; ++s) {
+        const int r = min(s * RPS + khalf, rows_valid - 1);
+        uint32_t w[KW];
+        load_words<KW>(sK + r * W + klane * KW, w);
+        float2 f[EK / 2];
+        unpack_words<BITS, EXACT_K, KW>(w, f);
+        const float4 ab = reinterpret_cast<const float4*>(sAB)[r * NG + gk];
+#pragma unroll
+        for (int h = 0; h < NH; h += 2) {
+          float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int k = 0; k < EK / 2; ++k) {
+            a0 = __ffma2_rn(f[k], qk[h][k], a0);
+            a1 = __ffma2_rn(f[k], qk[h + 1][k], a1);
+          }
+          const float2 sums = make_float2(a0.x + a0.y, a1.x + a1.y);
+          const float2 part = __ffma2_rn(make_float2(ab.x, ab.y), sums,
+                                         __fmul2_rn(make_float2(ab.z, ab.w), make_float2(qs[h], qs[h + 1])));
+          v[h * S + s] = part.x;
+          v[(h + 1) * S + s] = part.y;
+        }
+      }
+
+      // ---- phase 2: transposed butterfly over the LK lanes of a K row
+#pragma unroll
+      for (int k = 0; k < LOG_LK; ++k) {
+        const int n = NV >> k;
+        const bool upper = (lane >> k) & 1;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+          const float a = v[i], b = v[i + n / 2];
+          const float send = upper ? a : b;
+          const float keep = upper ? b : a;
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1 << k);
+        }
+      }
+
+      // ---- phase 3: block softmax for my head over my rows
+      float sc[NVL];
+      int rr[NVL];
+      float bm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < NVL; ++i) {
+        rr[i] = my_s[i] * RPS + khalf;
+        sc[i] = rr[i] < rows_valid ? v[i] : -INFINITY;
+        bm = fmaxf(bm, sc[i]);
+      }
+#pragma unroll
+      for (int off = NH; off < 32; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+      const float m_new = fmaxf(m_run, bm);
+      const float alpha = ex2(m_run - m_new);
+      const bool moved = __any_sync(0xffffffffu, m_new != m_run);
+      m_run = m_new;
+      float psum = 0.f;
+#pragma unroll
+      for (int g = 0; g < NG; ++g) pb[g] *= alpha;
+#pragma unroll
+      for (int i = 0; i < NVL; ++i) {
+        if (rr[i] < rows_valid) {
+          const float pr = ex2(sc[i] - m_new);
+          psum += pr;
+          const float* av = sAV + rr[i] * NG;
+          const float* bv = sBV + rr[i] * NG;
+          float2* ps = reinterpret_cast<float2*>(sPS) + (rr[i] * NG) * NH + my_h;
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            const float x = pr * av[g];
+            ps[g * NH] = make_float2(x, x);
+            pb[g] = fmaf(pr, bv[g], pb[g]);
+          }
+        }
+      }
+      l_run = fmaf(l_run, alpha, psum);
+      __syncwarp();
+
+      // ---- phase 4: V accumulation
+      if (moved) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const float a = __shfl_sync(0xffffffffu, alpha, head_lane[h]);
+#pragma unroll
+          for (int k = 0; k < EV / 2; ++k) o[h][k] = __fmul2_rn(o[h][k], make_float2(a, a));
+        }
+      }
+      const float4* psv = reinterpret_cast<const float4*>(sPS) + (gv * NH) / 2;
+      for (int r = 0; r < rows_valid; ++r) {
+        uint32_t w[VW];
+        load_words<VW>(sV + r * W + lane * VW, w);
+        float2 f[EV / 2];
+        unpack_words<BITS, EXACT, VW>(w, f);
+        const float4* pr = psv + (r * NG * NH) / 2;
+#pragma unroll
+        for (int h = 0; h < NH; h += 2) {
+          const float4 pp = pr[h / 2];   // (p A_v, p A_v) of heads h and h + 1
+#pragma unroll
+          for (int k = 0; k < EV / 2; ++k) {
+            o[h][k] = __ffma2_rn(make_float2(pp.x, pp.y), f[k], o[h][k]);
+            o[h + 1][k] = __ffma2_rn(make_float2(pp.z, pp.w), f[k], o[h + 1][k]);
+          }
+        }
+      }
+      __syncwarp();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+
+    if (c1 == walk.u_end || c1 == r1) {
+      // ------------------------------------------------------------- end of a segment
+      // l and the p * B_v sums: over all lanes owning the same head
+#pragma unroll
+      for (int off = NH; off < 32; off <<= 1) {
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
+#pragma unroll
+        for (int g = 0; g < NG; ++g) pb[g] += __shfl_xor_sync(0xffffffffu, pb[g], off);
+      }
+      if (lane < NH) {   // lane < NH owns head my_h; all heads are covered once
+#pragma unroll
+        for (int g = 0; g < NG; ++g) sPB[my_h * NG + g] = pb[g];
+      }
+      __syncwarp();
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const float b = sPB[h * NG + gv];
+#pragma unroll
+        for (int k = 0; k < EV / 2; ++k) o[h][k] = __fadd2_rn(o[h][k], make_float2(b, b));
+      }
+      named_barrier_sync(1, NW * 32);   // every warp is done with its scratch before it becomes the combine area
+#pragma unroll
+      for (int h = 0; h < NH; ++h)
+#pragma unroll
+        for (int k = 0; k < EV / 2; ++k)
+          reinterpret_cast<float2*>(comb_o + (warp * NH + h) * D + lane * EV)[k] = o[h][k];
+      if (lane < NH) {
+        comb_m[warp * NH + my_h] = m_run;
+        comb_l[warp * NH + my_h] = l_run;
+      }
+      named_barrier_sync(1, NW * 32);
+      const long long slot = (long long)cta + walk.unit;
+      for (int idx = threadIdx.x; idx < NH * D; idx += NW * 32) {
+        const int h = idx / D, d = idx - h * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, comb_m[w * NH + h]);
+        float O = 0.f, Ls = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float mw = comb_m[w * NH + h];
+          const float wt = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+          O = fmaf(comb_o[(w * NH + h) * D + d], wt, O);
+          Ls = fmaf(comb_l[w * NH + h], wt, Ls);
+        }
+        const size_t hp = (size_t)slot * p.heads_pad + (size_t)hc * NH + h;
+        p.part_o[hp * D + d] = O;
+        if (d == 0) p.part_ml[hp] = make_float2(M, Ls);
+      }
+      named_barrier_sync(1, NW * 32);
+    }
+    ++i_chunk;
+  }
+}
+
+template <int BITS, bool EXACT, typename Fn>
+cudaError_t with_split2_kernel(int D, int nh, int ng, Fn&& f) {
+#define QDA_V2(D_, NH_, NG_) \
+  if (D == D_ && nh == NH_ && ng == NG_) return f(qda_split2_kernel<BITS, D_, NH_, NG_, EXACT>);
+  QDA_V2(256, 2, 2) QDA_V2(256, 2, 4) QDA_V2(256, 2, 8)
+  QDA_V2(256, 4, 2) QDA_V2(256, 4, 4) QDA_V2(256, 4, 8)
+  QDA_V2(512, 2, 4) QDA_V2(512, 2, 8) QDA_V2(512, 2, 16)
+#undef QDA_V2
+  return cudaErrorInvalidValue;
+}
+
+template <int BITS, bool EXACT>
+cudaError_t launch_split2(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem, cudaStream_t s) {
+  return with_split2_kernel<BITS, EXACT>(D, nh, ng, [&](auto kern) -> cudaError_t {
+    cudaError_t e = ensure_smem_limit(kern, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, QDA_THREADS, smem, s>>>(p);
+    return cudaGetLastError();
+  });
+}
+
+template <int BITS, bool EXACT>
+cudaError_t occupancy_split2(int D, int nh, int ng, size_t smem, int* n) {
+  return with_split2_kernel<BITS, EXACT>(D, nh, ng, [&](auto kern) -> cudaError_t {
+    cudaError_t e = ensure_smem_limit(kern, smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, QDA_THREADS, smem);
+  });
+}
+
+}  // namespace qda

@@ -14,6 +14,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kStages = 4;
 constexpr size_t kStageTarget = 24 * 1024;   // bytes of K+V (codes, scales, biases) per pipeline stage
 constexpr long long kMinRowsPerCta = 128;
+constexpr long long kMaxCtas = 4096;   // the merge kernel stages one weight per partial in shared memory
 
 thread_local int t_last_cuda_error = 0;
 thread_local void* t_split_event = nullptr;
@@ -79,23 +80,47 @@ int check_dtype(int dtype, int* in, int* out) {
 }
 
 struct Variant {
+  int kind;              // 1: general split kernel, 2: lean kernel for D in {256, 512}
   int W, wpl, lpr, E, nh, hc, heads_pad, NG, tile, stages;
   size_t smem;
 };
 
+constexpr size_t kSmemBudget = 112 * 1024;   // two CTAs per SM
+
+// Rows per warp block of the lean kernel (its Split2Geom<...>::R).
+int split2_rows(int D, int nh) { return nh == 4 ? 8 : 16; }
+
 Variant pick_variant(int H, int Hkv, int D, int GS, int bits) {
   Variant v;
   v.W = D * bits / 32;
+  v.NG = D / GS;
+  const int nrep = H / Hkv;
+  const size_t row_bytes = 2 * (size_t)v.W * 4 + 4 * (size_t)v.NG * 2;
+  if (D == 256 || D == 512) {
+    v.kind = 2;
+    v.wpl = v.lpr = v.E = 0;
+    v.nh = (nrep <= 2 || D == 512) ? 2 : 4;   // D = 512 takes heads two at a time (register budget)
+    v.hc = (nrep + v.nh - 1) / v.nh;
+    v.heads_pad = v.hc * v.nh;
+    const int R = split2_rows(D, v.nh);
+    v.tile = R * QDA_NW;
+    const QdaSmemLayout L = qda_smem_layout(v.tile, 1, v.W, v.NG, v.nh, D);
+    const size_t scratch = (size_t)QDA_NW * split2_scratch_floats(R, v.NG, v.nh) * 4;
+    const size_t comb = (size_t)QDA_NW * v.nh * D * 4 + (size_t)QDA_NW * v.nh * 2 * 4;
+    const size_t tail = std::max(scratch, comb);
+    long long st = ((long long)kSmemBudget - (long long)L.stage0 - (long long)tail) / (long long)L.stage_bytes;
+    v.stages = (int)std::max(2LL, std::min(8LL, st));
+    v.smem = L.stage0 + (size_t)v.stages * L.stage_bytes + tail;
+    return v;
+  }
+  v.kind = 1;
   v.wpl = v.W > 32 ? v.W / 32 : 1;
   v.lpr = v.W > 32 ? 32 : v.W;
   v.E = v.wpl * (32 / bits);
-  const int nrep = H / Hkv;
   const int nh_max = std::min(8, 64 / v.E);
   v.nh = std::min(pow2ceil(nrep), nh_max);
   v.hc = (nrep + v.nh - 1) / v.nh;
   v.heads_pad = v.hc * v.nh;
-  v.NG = D / GS;
-  const size_t row_bytes = 2 * (size_t)v.W * 4 + 4 * (size_t)v.NG * 2;
   int tile = 256;
   while (tile > 16 && (size_t)tile * row_bytes > kStageTarget) tile >>= 1;
   v.tile = tile;
@@ -104,22 +129,30 @@ Variant pick_variant(int H, int Hkv, int D, int GS, int bits) {
   return v;
 }
 
-cudaError_t split_occupancy(int bits, bool f16, const Variant& v, int* n) {
-  if (bits == 4) {
-    return f16 ? qda_occupancy_split_b4_fp16(v.wpl, v.lpr, v.nh, v.smem, n)
-               : qda_occupancy_split_b4_bf16(v.wpl, v.lpr, v.nh, v.smem, n);
+cudaError_t split_occupancy(int bits, int D, bool exact, const Variant& v, int* n) {
+  if (v.kind == 2) {
+    if (bits == 4) {
+      return exact ? qda_occupancy_split2_b4_x1(D, v.nh, v.NG, v.smem, n)
+                   : qda_occupancy_split2_b4_x0(D, v.nh, v.NG, v.smem, n);
+    }
+    return exact ? qda_occupancy_split2_b8_x1(D, v.nh, v.NG, v.smem, n)
+                 : qda_occupancy_split2_b8_x0(D, v.nh, v.NG, v.smem, n);
   }
-  return f16 ? qda_occupancy_split_b8_fp16(v.wpl, v.lpr, v.nh, v.smem, n)
-             : qda_occupancy_split_b8_bf16(v.wpl, v.lpr, v.nh, v.smem, n);
+  return bits == 4 ? qda_occupancy_split1_b4(v.wpl, v.lpr, v.nh, v.smem, n)
+                   : qda_occupancy_split1_b8(v.wpl, v.lpr, v.nh, v.smem, n);
 }
 
-cudaError_t split_launch(int bits, bool f16, const QdaParams& p, const Variant& v, dim3 grid, cudaStream_t s) {
-  if (bits == 4) {
-    return f16 ? qda_launch_split_b4_fp16(p, v.wpl, v.lpr, v.nh, grid, v.smem, s)
-               : qda_launch_split_b4_bf16(p, v.wpl, v.lpr, v.nh, grid, v.smem, s);
+cudaError_t split_launch(int bits, bool exact, const QdaParams& p, const Variant& v, dim3 grid, cudaStream_t s) {
+  if (v.kind == 2) {
+    if (bits == 4) {
+      return exact ? qda_launch_split2_b4_x1(p, p.D, v.nh, v.NG, grid, v.smem, s)
+                   : qda_launch_split2_b4_x0(p, p.D, v.nh, v.NG, grid, v.smem, s);
+    }
+    return exact ? qda_launch_split2_b8_x1(p, p.D, v.nh, v.NG, grid, v.smem, s)
+                 : qda_launch_split2_b8_x0(p, p.D, v.nh, v.NG, grid, v.smem, s);
   }
-  return f16 ? qda_launch_split_b8_fp16(p, v.wpl, v.lpr, v.nh, grid, v.smem, s)
-             : qda_launch_split_b8_bf16(p, v.wpl, v.lpr, v.nh, grid, v.smem, s);
+  return bits == 4 ? qda_launch_split1_b4(p, v.wpl, v.lpr, v.nh, grid, v.smem, s)
+                   : qda_launch_split1_b8(p, v.wpl, v.lpr, v.nh, grid, v.smem, s);
 }
 
 // The plan: one contiguous, equal share of the flattened rows per CTA, as many CTAs as fit on the GPU at once
@@ -135,7 +168,7 @@ void make_plan(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits,
   long long C = std::min(target, by_rows);
   const int forced = g_force_splits.load();
   if (forced > 0) C = forced;
-  C = std::min<long long>(C, 1 << 20);
+  C = std::min<long long>(C, kMaxCtas);
   plan->num_ctas = (int)C;
   plan->head_chunks = v.hc;
   plan->heads_per_cta = v.nh;
@@ -175,15 +208,15 @@ DeviceState* device_state(int* dev_out) {
   return &d;
 }
 
-int occupancy_for(DeviceState& d, int bits, bool f16, const Variant& v, int* n) {
+int occupancy_for(DeviceState& d, int bits, int D, bool exact, const Variant& v, int* n) {
   std::lock_guard<std::mutex> lock(d.mu);
-  auto key = std::make_tuple(bits, (int)f16, v.wpl, v.lpr, v.nh, v.smem);
+  auto key = std::make_tuple(bits + 16 * (int)exact + 64 * v.kind, D, v.wpl * 64 + v.lpr, v.nh, v.NG, v.smem);
   auto it = d.occupancy.find(key);
   if (it != d.occupancy.end()) {
     *n = it->second;
     return QDA_OK;
   }
-  cudaError_t e = split_occupancy(bits, f16, v, n);
+  cudaError_t e = split_occupancy(bits, D, exact, v, n);
   if (e != cudaSuccess) return cuda_fail(e);
   if (*n < 1) *n = 1;
   d.occupancy[key] = *n;
@@ -207,7 +240,7 @@ int qdecode_attn_plan(int B, int H, int Hkv, const int32_t* N, int D, int GS, in
     if (num_sms <= 0) num_sms = d->num_sms;
     if (ctas_per_sm <= 0) {
       // the input dtype does not change the kernel's resources; bf16 stands for both
-      st = occupancy_for(*d, bits, false, v, &ctas_per_sm);
+      st = occupancy_for(*d, bits, D, false, v, &ctas_per_sm);
       if (st != QDA_OK) return st;
     }
   }
@@ -266,7 +299,8 @@ int qdecode_attn(const void* q, const uint32_t* k_packed, const void* k_scales, 
   const bool f16 = in_dt == QDA_FP16;
   const Variant v = pick_variant(H, Hkv, D, GS, bits);
   int occ = 1;
-  st = occupancy_for(*d, bits, f16, v, &occ);
+  const bool exact = out_dt == QDA_FP32;
+  st = occupancy_for(*d, bits, D, exact, v, &occ);
   if (st != QDA_OK) return st;
   qda_plan plan;
   make_plan(B, H, Hkv, N, D, GS, bits, d->num_sms, occ, v, &plan);
@@ -314,15 +348,17 @@ int qdecode_attn(const void* q, const uint32_t* k_packed, const void* k_scales, 
   p.W = v.W;
   p.nrep = H / Hkv;
   p.heads_pad = v.heads_pad;
+  p.head_chunks = v.hc;
   p.num_ctas = plan.num_ctas;
   p.tile_rows = v.tile;
   p.stages = v.stages;
+  p.f16 = f16 ? 1 : 0;
   p.qscale = 1.4426950408889634f / sqrtf((float)D);
   p.seq_off[0] = 0;
   for (int b = 0; b < B; ++b) p.seq_off[b + 1] = p.seq_off[b] + N[b];
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = split_launch(bits, f16, p, v, dim3((unsigned)plan.num_ctas, (unsigned)v.hc), s);
+  cudaError_t e = split_launch(bits, exact, p, v, dim3((unsigned)plan.num_ctas * (unsigned)v.hc), s);
   if (e != cudaSuccess) return cuda_fail(e);
   const bool use_event = t_split_event != nullptr;
   if (use_event) {

@@ -74,7 +74,7 @@ def measured_peaks():
 
 def split_kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in ("qda_split.cuh", "qda_ptx.cuh", "qda_internal.h", "qdecode_attn.cu"):
+    for f in ("qda_split.cuh", "qda_split2.cuh", "qda_ptx.cuh", "qda_internal.h", "qdecode_attn.cu"):
         with open(os.path.join(ROOT, "attention_quantized_kv_split_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -254,8 +254,7 @@ def run_ours(args):
     def flush():
         flush_buf.zero_()
 
-    def call():
-        qda.decode_attention(q, cache, out=out)
+    call = qda.bind_decode_attention(q, cache, out, stream)
 
     plan = qda.qdecode_attn_plan(w.B, w.H, w.Hkv, N, w.D, w.GS, w.bits)
     for _ in range(max(3, args.warmup)):
@@ -313,7 +312,7 @@ def run_ours(args):
     achieved = nbytes / (split_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
-                "kernel": "qda_split_kernel", "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                "kernel": "qda_split2_kernel" if w.D in (256, 512) else "qda_split_kernel", "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6800 GB/s",
                 "split_kernel_us": round(split_ms * 1e3, 3), "merge_kernel_us": round(merge_ms * 1e3, 3),
                 "algorithmic_bytes_per_launch": nbytes}
@@ -351,7 +350,7 @@ def run_ours(args):
             wx = synth.workload(idx)
             Nx, qx, cx = make_workload(wx, device)
             ox = torch.empty((wx.B, wx.H, wx.D), dtype=synth.DT[wx.dtype_out], device=device)
-            fx = lambda: qda.decode_attention(qx, cx, out=ox)  # noqa: E731
+            fx = qda.bind_decode_attention(qx, cx, ox, stream)
             for _ in range(5):
                 fx()
             msx = time_calls(fx, 50, flush, stream)
