@@ -25,6 +25,7 @@ struct QdaParams {
   unsigned int* err;          // device error word
   long long total_rows;       // T = Hkv * sum(N)
   int B, H, Hkv, D, GS, NG, W, nrep, heads_pad, head_chunks, num_ctas, tile_rows, stages;
+  int tile_shift;             // log2(tile_rows): pipeline tiles are powers of two
   int f16;                    // q / scales / biases are fp16 (else bf16)
   float qscale;               // log2(e) / sqrt(D): scores come out in log2 units
   int seq_off[QDA_MAX_B + 1]; // seq_off[b] = N[0] + ... + N[b-1]
@@ -69,9 +70,10 @@ __host__ __device__ inline QdaSmemLayout qda_smem_layout(int tile_rows, int stag
 }
 
 // Lean split kernel: floats of per-warp scratch (K coefficients (A, A, B, B) and V coefficients A_v, B_v per
-// (row, group), p * A_v pairs per (row, group, head), per-head sums of p * B_v per group).
+// (row, group), p * A_v pairs per (row, head, group) with one float4 of padding per row, per-head sums of p * B_v
+// per group).
 __host__ __device__ inline int split2_scratch_floats(int R, int NG, int NH) {
-  return R * NG * (4 + 2 + 2 * NH) + NH * NG;
+  return R * NG * (4 + 2) + R * ((NH / 2) * NG + 1) * 4 + NH * NG;
 }
 
 // Launchers of the split kernels, one translation unit per (kernel, bits[, exact]). They return cudaSuccess or the

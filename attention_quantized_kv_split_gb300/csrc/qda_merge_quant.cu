@@ -33,19 +33,17 @@ __device__ __forceinline__ void store4(void* out, size_t idx, float4 v) {
 }
 
 // out[b, h, :] = sum_s o_s 2^(m_s - M) / sum_s l_s 2^(m_s - M) over the partial slots of (b, KV head of h)
-// (mlx-bun fused-decode-kernel.ts, MERGE_SOURCE), in log2 units. One CTA per (b, h). The slot weights are staged
-// in shared memory once; the o rows are dealt to 256 / (D/4) thread groups round-robin and every sum runs in a
-// fixed order, so the result is deterministic without atomics.
-constexpr int kMergeThreads = 256;
-constexpr int kMergeMaxSlots = 4096;
+// (mlx-bun fused-decode-kernel.ts, MERGE_SOURCE), in log2 units. One CTA per (b, h). The slots are dealt to
+// kMergeThreads / (D/4) thread groups round-robin; each thread folds its slots in one pass with a running max, so
+// the (m, l) and o loads of a slot are issued together, and the groups are then combined in a fixed order:
+// deterministic, no atomics.
+constexpr int kMergeThreads = 512;
 
 template <int OUT>
 __global__ void __launch_bounds__(kMergeThreads) qda_merge_kernel(const __grid_constant__ QdaParams p,
                                                                   void* __restrict__ out) {
-  __shared__ float s_w[kMergeMaxSlots];   // slot max, then slot weight 2^(m_s - M) (0 for an empty range)
-  __shared__ float s_l[kMergeMaxSlots];   // slot sum, then weighted
-  __shared__ float4 red[kMergeThreads];
-  __shared__ float redf[kMergeThreads];
+  __shared__ float4 red_o[kMergeThreads];
+  __shared__ float2 red_ml[kMergeThreads];
   const int tid = threadIdx.x;
   const int D = p.D;
   const int bh = blockIdx.x;
@@ -58,74 +56,57 @@ __global__ void __launch_bounds__(kMergeThreads) qda_merge_kernel(const __grid_c
   const int C = p.num_ctas;
   const int cf = qda_cta_of(T, C, us);
   const int ns = qda_cta_of(T, C, us + n - 1) - cf + 1;
-
-  pdl_wait();   // the split kernel's partials are complete and visible from here on
-
-  // slot statistics; CTAs with an empty row range (ranges shorter than 8 rows) wrote no slot
-  float mx = -INFINITY;
-  for (int k = tid; k < ns; k += kMergeThreads) {
-    const int c = cf + k;
-    float m = -INFINITY, l = 0.f;
-    if (qda_cta_row(T, C, c) != qda_cta_row(T, C, c + 1)) {
-      const float2 ml = p.part_ml[(size_t)(c + unit) * p.heads_pad + j];
-      m = ml.x;
-      l = ml.y;
-    }
-    s_w[k] = m;
-    s_l[k] = l;
-    mx = fmaxf(mx, m);
-  }
-  redf[tid] = mx;
-  __syncthreads();
-  for (int w = kMergeThreads / 2; w > 0; w >>= 1) {
-    if (tid < w) redf[tid] = fmaxf(redf[tid], redf[tid + w]);
-    __syncthreads();
-  }
-  const float M = redf[0];
-  __syncthreads();
-  float den = 0.f;
-  for (int k = tid; k < ns; k += kMergeThreads) {
-    const float wt = ex2m(s_w[k] - M);   // 2^-inf = 0 for empty slots
-    s_w[k] = wt;
-    den = fmaf(s_l[k], wt, den);
-  }
-  redf[tid] = den;
-  __syncthreads();
-  for (int w = kMergeThreads / 2; w > 0; w >>= 1) {
-    if (tid < w) redf[tid] += redf[tid + w];
-    __syncthreads();
-  }
-  const float inv = 1.0f / redf[0];
-
+  const bool maybe_empty = T / C < 8;   // only ranges shorter than 8 rows can be empty (and wrote no slot)
   const int tpr = D >> 2;
   const int groups = kMergeThreads / tpr;
   const int grp = tid / tpr, t = tid - grp * tpr;
+
+  pdl_wait();   // the split kernel's partials are complete and visible from here on
+
+  float m_run = -INFINITY, den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
   for (int k = grp; k < ns; k += groups) {
-    const float wt = s_w[k];
-    if (wt == 0.f) continue;
-    const size_t hp = (size_t)(cf + k + unit) * p.heads_pad + j;
+    const int c = cf + k;
+    const size_t hp = (size_t)(c + unit) * p.heads_pad + j;
+    const float2 ml = p.part_ml[hp];
     const float4 v = reinterpret_cast<const float4*>(p.part_o + hp * D)[t];
-    acc.x = fmaf(v.x, wt, acc.x);
-    acc.y = fmaf(v.y, wt, acc.y);
-    acc.z = fmaf(v.z, wt, acc.z);
-    acc.w = fmaf(v.w, wt, acc.w);
+    if (maybe_empty && qda_cta_row(T, C, c) == qda_cta_row(T, C, c + 1)) continue;
+    const float mn = fmaxf(m_run, ml.x);
+    const float a = ex2m(m_run - mn);   // 0 on the first slot
+    const float w = ex2m(ml.x - mn);
+    den = fmaf(den, a, ml.y * w);
+    acc.x = fmaf(acc.x, a, v.x * w);
+    acc.y = fmaf(acc.y, a, v.y * w);
+    acc.z = fmaf(acc.z, a, v.z * w);
+    acc.w = fmaf(acc.w, a, v.w * w);
+    m_run = mn;
   }
-  red[tid] = acc;
+  red_o[tid] = acc;
+  if (t == 0) red_ml[grp] = make_float2(m_run, den);
   __syncthreads();
   if (grp != 0) return;
-  for (int g = 1; g < groups; ++g) {
-    const float4 v = red[g * tpr + t];
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
+  float M = -INFINITY;
+  for (int g = 0; g < groups; ++g) M = fmaxf(M, red_ml[g].x);
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  float dt = 0.f;
+  for (int g = 0; g < groups; ++g) {
+    const float2 ml = red_ml[g];
+    if (ml.x == -INFINITY) continue;   // a group that held no slot
+    const float w = ex2m(ml.x - M);
+    const float4 v = red_o[g * tpr + t];
+    dt = fmaf(ml.y, w, dt);
+    o.x = fmaf(v.x, w, o.x);
+    o.y = fmaf(v.y, w, o.y);
+    o.z = fmaf(v.z, w, o.z);
+    o.w = fmaf(v.w, w, o.w);
   }
-  acc.x *= inv;
-  acc.y *= inv;
-  acc.z *= inv;
-  acc.w *= inv;
-  store4<OUT>(out, ((size_t)bh * D >> 2) + t, acc);
+  const float inv = 1.0f / dt;
+  o.x *= inv;
+  o.y *= inv;
+  o.z *= inv;
+  o.w *= inv;
+  store4<OUT>(out, ((size_t)bh * D >> 2) + t, o);
 }
 
 // ------------------------------------------------------------------------------------------- quantizer

@@ -63,7 +63,7 @@ struct ChunkWalker {
       u_end = u_start + n;
       unit = b * p.Hkv + kvh;
     }
-    t0 = (r / p.tile_rows) * p.tile_rows;
+    t0 = (r >> p.tile_shift) << p.tile_shift;
     c0 = r;
     c1 = min(min(t0 + (long long)p.tile_rows, u_end), r_end);
     r = c1;

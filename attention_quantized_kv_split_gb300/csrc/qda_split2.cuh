@@ -191,8 +191,11 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
   float* sAB = scratch_all + warp * sw_floats;          // [R][NG] float4 (A, A, B, B) of K
   float* sAV = sAB + R * NG * 4;                        // [R][NG] A_v
   float* sBV = sAV + R * NG;                            // [R][NG] B_v
-  float* sPS = sBV + R * NG;                            // [R][NG][NH] float2 (p A_v, p A_v)
-  float* sPB = sPS + R * NG * NH * 2;                   // [NH][NG]
+  // p * A_v as float4 (pA_h, pA_h, pA_h+1, pA_h+1) per (row, head pair, group), rows padded by one float4 so
+  // that the owners of different rows write to different banks
+  float* sPS = sBV + R * NG;
+  constexpr int PS_ROW = (NH / 2) * NG + 1;             // float4 per row
+  float* sPB = sPS + R * PS_ROW * 4;                    // [NH][NG]
 
   const int klane = lane & (LK - 1);                    // K slice: codes [klane*EK, klane*EK + EK)
   const int khalf = lane / LK;                          // which row of a K step
@@ -299,12 +302,18 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
         const float4 ab = reinterpret_cast<const float4*>(sAB)[r * NG + gk];
 #pragma unroll
         for (int h = 0; h < NH; h += 2) {
+          // four independent chains of EK/4 packed FMAs (even and odd pairs of codes, two heads)
           float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+          float2 b0 = make_float2(0.f, 0.f), b1 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int k = 0; k < EK / 2; ++k) {
+          for (int k = 0; k < EK / 2; k += 2) {
             a0 = __ffma2_rn(f[k], qk[h][k], a0);
             a1 = __ffma2_rn(f[k], qk[h + 1][k], a1);
+            b0 = __ffma2_rn(f[k + 1], qk[h][k + 1], b0);
+            b1 = __ffma2_rn(f[k + 1], qk[h + 1][k + 1], b1);
           }
+          a0 = __fadd2_rn(a0, b0);
+          a1 = __fadd2_rn(a1, b1);
           const float2 sums = make_float2(a0.x + a0.y, a1.x + a1.y);
           const float2 part = __ffma2_rn(make_float2(ab.x, ab.y), sums,
                                          __fmul2_rn(make_float2(ab.z, ab.w), make_float2(qs[h], qs[h + 1])));
@@ -353,11 +362,11 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
           psum += pr;
           const float* av = sAV + rr[i] * NG;
           const float* bv = sBV + rr[i] * NG;
-          float2* ps = reinterpret_cast<float2*>(sPS) + (rr[i] * NG) * NH + my_h;
+          float2* ps = reinterpret_cast<float2*>(sPS) + 2 * (rr[i] * PS_ROW + (my_h >> 1) * NG) + (my_h & 1);
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
             const float x = pr * av[g];
-            ps[g * NH] = make_float2(x, x);
+            ps[2 * g] = make_float2(x, x);
             pb[g] = fmaf(pr, bv[g], pb[g]);
           }
         }
@@ -374,16 +383,18 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
           for (int k = 0; k < EV / 2; ++k) o[h][k] = __fmul2_rn(o[h][k], make_float2(a, a));
         }
       }
-      const float4* psv = reinterpret_cast<const float4*>(sPS) + (gv * NH) / 2;
-      for (int r = 0; r < rows_valid; ++r) {
+      const float4* psv = reinterpret_cast<const float4*>(sPS) + gv;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (r >= rows_valid) break;   // warp-uniform
         uint32_t w[VW];
         load_words<VW>(sV + r * W + lane * VW, w);
         float2 f[EV / 2];
         unpack_words<BITS, EXACT, VW>(w, f);
-        const float4* pr = psv + (r * NG * NH) / 2;
+        const float4* pr = psv + r * PS_ROW;
 #pragma unroll
         for (int h = 0; h < NH; h += 2) {
-          const float4 pp = pr[h / 2];   // (p A_v, p A_v) of heads h and h + 1
+          const float4 pp = pr[(h / 2) * NG];   // (p A_v, p A_v) of heads h and h + 1
 #pragma unroll
           for (int k = 0; k < EV / 2; ++k) {
             o[h][k] = __ffma2_rn(make_float2(pp.x, pp.y), f[k], o[h][k]);

@@ -352,6 +352,8 @@ int qdecode_attn(const void* q, const uint32_t* k_packed, const void* k_scales, 
   p.num_ctas = plan.num_ctas;
   p.tile_rows = v.tile;
   p.stages = v.stages;
+  p.tile_shift = 0;
+  while ((1 << p.tile_shift) < v.tile) ++p.tile_shift;
   p.f16 = f16 ? 1 : 0;
   p.qscale = 1.4426950408889634f / sqrtf((float)D);
   p.seq_off[0] = 0;
