@@ -52,6 +52,20 @@ def qdecode_attn(q: torch.Tensor, k_packed: torch.Tensor, k_scales: torch.Tensor
     return out
 
 
+def qdecode_attn_noalloc(q: torch.Tensor, k_packed: torch.Tensor, k_scales: torch.Tensor, k_biases: torch.Tensor,
+                         v_packed: torch.Tensor, v_scales: torch.Tensor, v_biases: torch.Tensor, out: torch.Tensor,
+                         N: Sequence[int], Hkv: int, GS: int, bits: int, stream=None) -> torch.Tensor:
+    """qdecode_attn for callers that must not allocate device memory: the library's fixed scratch array is used
+    instead of a workspace (shapes needing more than QDA_STATIC_SCRATCH_BYTES are rejected). Calls that overlap
+    on the GPU share that array and must be serialised by the caller."""
+    B, H, D = q.shape
+    st = lib().qdecode_attn_noalloc(_ptr(q), _ptr(k_packed), _ptr(k_scales), _ptr(k_biases), _ptr(v_packed),
+                                    _ptr(v_scales), _ptr(v_biases), _ptr(out), B, H, Hkv, _lib.int32_array(N), D,
+                                    GS, bits, dtype_code(q.dtype, out.dtype), _stream(stream))
+    _lib.check(st, "qdecode_attn_noalloc")
+    return out
+
+
 def bind_qdecode_attn(q: torch.Tensor, k_packed: torch.Tensor, k_scales: torch.Tensor, k_biases: torch.Tensor,
                       v_packed: torch.Tensor, v_scales: torch.Tensor, v_biases: torch.Tensor, out: torch.Tensor,
                       N: Sequence[int], Hkv: int, GS: int, bits: int, stream=None):

@@ -14,6 +14,8 @@ QDA_ERR_UNSUPPORTED = -2
 QDA_ERR_ALIGN = -3
 QDA_ERR_CUDA = -4
 QDA_ERR_WORKSPACE = -5
+QDA_ERR_SCRATCH = -6
+QDA_STATIC_SCRATCH_BYTES = 8 << 20
 QDA_BF16, QDA_FP16, QDA_FP32 = 1, 2, 3
 QDA_MAX_B = 512
 QDA_MAX_NREP = 64
@@ -43,6 +45,7 @@ _PI32 = ctypes.POINTER(ctypes.c_int32)
 
 SIGNATURES = {
     "qdecode_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _PI32, _I, _I, _I, _I, _P]),
+    "qdecode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _PI32, _I, _I, _I, _I, _P]),
     "qdecode_attn_plan": (_I, [_I, _I, _I, _PI32, _I, _I, _I, _I, _I, ctypes.POINTER(QdaPlan)]),
     "qdecode_attn_workspace_bytes": (_I, [_I, _I, _I, _PI32, _I, _I, _I, ctypes.POINTER(_SZ)]),
     "qdecode_attn_set_workspace": (_I, [_P, _SZ]),

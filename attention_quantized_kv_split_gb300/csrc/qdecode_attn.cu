@@ -401,6 +401,7 @@ const char* qdecode_attn_strerror(int status) {
     case QDA_ERR_ALIGN: return "a data pointer is not 16-byte aligned";
     case QDA_ERR_CUDA: return "CUDA runtime error (see qdecode_attn_last_cuda_error)";
     case QDA_ERR_WORKSPACE: return "installed workspace is too small for this call";
+    case QDA_ERR_SCRATCH: return "call needs more scratch than the fixed array of qdecode_attn_noalloc holds";
     default: return "unknown status";
   }
 }
@@ -425,3 +426,95 @@ int qdecode_attn_device_status(unsigned int* flags) {
 long long qdecode_attn_calls(void) { return g_calls.load(); }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------------------------
+// Allocation-free entry point. Its partial results live in this fixed device array instead of a cudaMalloc'ed
+// workspace. Host code must not pass the array's name to a kernel (on the host it names a stand-in, not device
+// memory): the device address is looked up once per device with cudaGetSymbolAddress and cached.
+namespace {
+static __device__ __align__(256) unsigned char g_qda_static_scratch[QDA_STATIC_SCRATCH_BYTES];
+std::mutex g_static_mu;
+void* g_static_scratch_addr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" int qdecode_attn_noalloc(const void* q, const uint32_t* k_packed, const void* k_scales,
+                                    const void* k_biases, const uint32_t* v_packed, const void* v_scales,
+                                    const void* v_biases, void* out, int B, int H, int Hkv, const int32_t* N,
+                                    int D, int GS, int bits, int dtype, void* stream) {
+  if (!q || !k_packed || !k_scales || !k_biases || !v_packed || !v_scales || !v_biases || !out)
+    return QDA_ERR_INVALID;
+  int in_dt, out_dt;
+  int st = check_dtype(dtype, &in_dt, &out_dt);
+  if (st != QDA_OK) return st;
+  st = check_shape(B, H, Hkv, N, D, GS, bits);
+  if (st != QDA_OK) return st;
+  const void* ptrs[8] = {q, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, out};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return QDA_ERR_ALIGN;
+
+  int dev;
+  DeviceState* d = device_state(&dev);
+  if (d == nullptr) return QDA_ERR_CUDA;
+  const Variant v = pick_variant(H, Hkv, D, GS, bits);
+  const bool exact = out_dt == QDA_FP32;
+  int occ = 1;
+  st = occupancy_for(*d, bits, D, exact, v, &occ);
+  if (st != QDA_OK) return st;
+  qda_plan plan;
+  make_plan(B, H, Hkv, N, D, GS, bits, d->num_sms, occ, v, &plan);
+  if (plan.workspace_bytes > (size_t)QDA_STATIC_SCRATCH_BYTES) return QDA_ERR_SCRATCH;
+
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_scratch_addr[dev] == nullptr) {
+      void* ptr = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&ptr, g_qda_static_scratch);
+      if (e != cudaSuccess) return cuda_fail(e);
+      g_static_scratch_addr[dev] = ptr;
+    }
+    scratch = g_static_scratch_addr[dev];
+  }
+
+  QdaParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q;
+  p.kp = k_packed;
+  p.ks = static_cast<const uint16_t*>(k_scales);
+  p.kb = static_cast<const uint16_t*>(k_biases);
+  p.vp = v_packed;
+  p.vs = static_cast<const uint16_t*>(v_scales);
+  p.vb = static_cast<const uint16_t*>(v_biases);
+  const size_t o_bytes = (size_t)plan.slots * v.heads_pad * D * sizeof(float);
+  p.part_o = static_cast<float*>(scratch);
+  p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(scratch) + ((o_bytes + 255) & ~(size_t)255));
+  p.err = d->err;
+  p.total_rows = plan.total_rows;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.GS = GS;
+  p.NG = v.NG;
+  p.W = v.W;
+  p.nrep = H / Hkv;
+  p.heads_pad = v.heads_pad;
+  p.head_chunks = v.hc;
+  p.num_ctas = plan.num_ctas;
+  p.tile_rows = v.tile;
+  p.stages = v.stages;
+  p.tile_shift = 0;
+  while ((1 << p.tile_shift) < v.tile) ++p.tile_shift;
+  p.f16 = in_dt == QDA_FP16 ? 1 : 0;
+  p.qscale = 1.4426950408889634f / sqrtf((float)D);
+  p.seq_off[0] = 0;
+  for (int b = 0; b < B; ++b) p.seq_off[b + 1] = p.seq_off[b] + N[b];
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = split_launch(bits, exact, p, v, dim3((unsigned)plan.num_ctas * (unsigned)v.hc), s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = qda_launch_merge(p, out, out_dt, true, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_calls.fetch_add(1);
+  return QDA_OK;
+}

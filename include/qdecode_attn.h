@@ -50,6 +50,7 @@ extern "C" {
 #define QDA_ERR_ALIGN (-3)       /* a data pointer is not 16-byte aligned */
 #define QDA_ERR_CUDA (-4)        /* CUDA runtime error; see qdecode_attn_last_cuda_error() */
 #define QDA_ERR_WORKSPACE (-5)   /* the caller-provided workspace is smaller than the call needs */
+#define QDA_ERR_SCRATCH (-6)     /* qdecode_attn_noalloc: the call needs more scratch than QDA_STATIC_SCRATCH_BYTES */
 
 #define QDA_BF16 1
 #define QDA_FP16 2
@@ -72,6 +73,27 @@ extern "C" {
 int qdecode_attn(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
                  const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out,
                  int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream);
+
+/*
+ * qdecode_attn_noalloc: the same operation, arguments, layouts and result as qdecode_attn, for callers that are not
+ * allowed to allocate device memory at all -- for example code running under an allocator that owns the whole
+ * device, a real-time loop where cudaMalloc's implicit device synchronisation is not acceptable, or a host that
+ * hands this library only pre-allocated buffers. (The pages this library follows have no counterpart of this
+ * entry point.)
+ *
+ * Its scratch space for the per-range partial results is a fixed array of QDA_STATIC_SCRATCH_BYTES compiled into
+ * the library: every GPU that loads the library holds that much device memory until the process exits. No call
+ * allocates or frees anything. A shape whose scratch need (qdecode_attn_workspace_bytes) exceeds the array is
+ * rejected with QDA_ERR_SCRATCH before anything is launched. The first call on a device looks up the array's
+ * device address and caches it (and sets the kernels' shared-memory limits): make that first call before any
+ * stream capture on that device. The array is shared by every call on a device and keeps the previous call's
+ * contents; nothing in it needs to start at zero, but calls whose kernels overlap on the GPU (different streams,
+ * no ordering between them) race on it and must be serialised by the caller.
+ */
+#define QDA_STATIC_SCRATCH_BYTES (8u << 20)
+int qdecode_attn_noalloc(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
+                         const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out,
+                         int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream);
 
 /* The launch plan qdecode_attn would use (host only). Determined by the shape and the GPU alone. */
 typedef struct {
