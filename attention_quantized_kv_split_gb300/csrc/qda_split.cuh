@@ -80,21 +80,27 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   }
 }
 
-// The producer lane: walks the CTA's chunks and fills the shared-memory ring. Per chunk: the K and V codes of its
+// The producer warp: walks the CTA's chunks and fills the shared-memory ring. Per chunk: the K and V codes of its
 // rows and the 8-row aligned cover of its scales/biases (clipped to the arrays' end; a ragged last < 16 bytes go
-// by plain loads, published by the arrive), all completing on full[stage]. Waits for the consumers to free a
-// stage (empty[stage]) before reusing it; before returning it waits until every copy it issued has landed.
+// by plain loads, published by the arrive), all completing on full[stage]. Lane 0 waits for the consumers to
+// free a stage (empty[stage]) and posts the byte count; lanes 0..5 then issue the six copies side by side. Before
+// returning, lane 0 waits until every copy the warp issued has landed. Called by all 32 lanes of the warp.
 __device__ __forceinline__ void produce_range(const QdaParams& p, ChunkWalker walk, unsigned char* smem,
                                               const QdaSmemLayout& L, uint64_t* full, uint64_t* empty,
                                               volatile int* abort_flag, long long T) {
+  const int lane = threadIdx.x & 31;
   const int STAGES = p.stages, NG = p.NG, W = p.W;
   const uint64_t pol = policy_evict_first();
   const uint32_t RB = W * 4, SB = NG * 2;
   long long c0, c1, t0;
   int i = 0;
+  int s = 0, ph = 0;   // ring slot of chunk i and the parity of its use (i / STAGES) & 1
   while (walk.next(p, c0, c1, t0)) {
-    const int s = i % STAGES;
-    if (i >= STAGES && !mbar_wait_bounded(&empty[s], ((i / STAGES) - 1) & 1, abort_flag, p.err, 1u)) break;
+    if (i >= STAGES) {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, p.err, 1u);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    }
     unsigned char* st = smem + L.stage0 + (size_t)s * L.stage_bytes;
     const uint32_t cbytes = (uint32_t)(c1 - c0) * RB;
     const size_t coff = (size_t)(c0 - t0) * RB;
@@ -103,24 +109,35 @@ __device__ __forceinline__ void produce_range(const QdaParams& p, ChunkWalker wa
     const uint32_t sbytes = (uint32_t)(s1 - s0) * SB;
     const uint32_t s16 = sbytes & ~15u;
     const size_t soff = (size_t)(s0 - t0) * SB;
-    const uint16_t* srcs[4] = {p.ks, p.kb, p.vs, p.vb};
-    if (s16 != sbytes) {
-      for (int a = 0; a < 4; ++a) {
-        const uint16_t* src = srcs[a] + s0 * NG + s16 / 2;
-        uint16_t* dst = reinterpret_cast<uint16_t*>(st + 2 * L.codes_bytes + a * L.sc_bytes + soff + s16);
-        for (uint32_t k = 0; k < (sbytes - s16) / 2; ++k) dst[k] = src[k];
+    if (lane == 0) {
+      if (s16 != sbytes) {
+        const uint16_t* srcs[4] = {p.ks, p.kb, p.vs, p.vb};
+        for (int a = 0; a < 4; ++a) {
+          const uint16_t* src = srcs[a] + s0 * NG + s16 / 2;
+          uint16_t* dst = reinterpret_cast<uint16_t*>(st + 2 * L.codes_bytes + a * L.sc_bytes + soff + s16);
+          for (uint32_t k = 0; k < (sbytes - s16) / 2; ++k) dst[k] = src[k];
+        }
       }
+      mbar_arrive_expect_tx(&full[s], 2 * cbytes + 4 * s16);
     }
-    mbar_arrive_expect_tx(&full[s], 2 * cbytes + 4 * s16);
-    bulk_g2s(st + coff, p.kp + c0 * W, cbytes, &full[s], pol);
-    bulk_g2s(st + L.codes_bytes + coff, p.vp + c0 * W, cbytes, &full[s], pol);
-    if (s16) {
-      for (int a = 0; a < 4; ++a)
-        bulk_g2s(st + 2 * L.codes_bytes + a * L.sc_bytes + soff, srcs[a] + s0 * NG, s16, &full[s], pol);
+    __syncwarp();
+    if (lane == 0) {
+      bulk_g2s(st + coff, p.kp + c0 * W, cbytes, &full[s], pol);
+    } else if (lane == 1) {
+      bulk_g2s(st + L.codes_bytes + coff, p.vp + c0 * W, cbytes, &full[s], pol);
+    } else if (lane < 6 && s16) {
+      const int a = lane - 2;
+      const uint16_t* src = a == 0 ? p.ks : a == 1 ? p.kb : a == 2 ? p.vs : p.vb;
+      bulk_g2s(st + 2 * L.codes_bytes + a * L.sc_bytes + soff, src + s0 * NG, s16, &full[s], pol);
     }
     ++i;
+    if (++s == STAGES) {
+      s = 0;
+      ph ^= 1;
+    }
   }
-  for (int j = (i > STAGES ? i - STAGES : 0); j < i; ++j) mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1, p.err);
+  if (lane == 0)
+    for (int j = (i > STAGES ? i - STAGES : 0); j < i; ++j) mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1, p.err);
 }
 
 // BITS: 4 or 8. WPL: packed words per lane per row. LPR: lanes per row (RPS = 32/LPR rows per warp step).
@@ -170,7 +187,7 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
   long long c0, c1, t0;
 
   if (warp == NW) {
-    if (lane == 0) produce_range(p, walk, smem, L, full, empty, abort_flag, T);
+    produce_range(p, walk, smem, L, full, empty, abort_flag, T);
     return;
   }
 
@@ -179,7 +196,7 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
   const int lir = lane % LPR;     // lane's slice of the row: elements [lir*E, lir*E + E)
   float qv[NH][E], qsum[NH], o[NH][E], m[NH], l[NH];
   int cur_unit = -1;
-  int i = 0;
+  int s = 0, phase = 0;   // ring slot of the current chunk and the parity of its use
   while (walk.next(p, c0, c1, t0)) {
     if (walk.unit != cur_unit) {  // a new (sequence, KV head): load its query heads, reset the softmax state
       cur_unit = walk.unit;
@@ -206,8 +223,7 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
         for (int e = 0; e < E; ++e) o[h][e] = 0.f;
       }
     }
-    const int s = i % STAGES;
-    const bool ok = mbar_wait_bounded(&full[s], (i / STAGES) & 1, abort_flag, p.err, 1u);
+    const bool ok = mbar_wait_bounded(&full[s], phase, abort_flag, p.err, 1u);
     if (ok) {
       const unsigned char* st = smem + L.stage0 + (size_t)s * L.stage_bytes;
       const uint32_t* sK = reinterpret_cast<const uint32_t*>(st);
@@ -332,7 +348,10 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
       }
       named_barrier_sync(1, NW * 32);
     }
-    ++i;
+    if (++s == STAGES) {
+      s = 0;
+      phase ^= 1;
+    }
   }
 }
 

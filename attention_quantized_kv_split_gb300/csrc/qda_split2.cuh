@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
   long long c0, c1, t0;
 
   if (warp == NW) {
-    if (lane == 0) produce_range(p, walk, smem, L, full, empty, abort_flag, T);
+    produce_range(p, walk, smem, L, full, empty, abort_flag, T);
     return;
   }
 
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
   float l_run = 0.f;        // sum of 2^(s - m_run) over my rows
   float pb[NG];             // sum of p * B_v per group, my head
   int cur_unit = -1;
-  int i_chunk = 0;
+  int stage = 0, phase = 0;   // ring slot of the current chunk and the parity of its use
 
   while (walk.next(p, c0, c1, t0)) {
     if (walk.unit != cur_unit) {
@@ -266,11 +266,10 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       for (int g = 0; g < NG; ++g) pb[g] = 0.f;
     }
 
-    const int stage = i_chunk % STAGES;
-    const bool ok = mbar_wait_bounded(&full[stage], (i_chunk / STAGES) & 1, abort_flag, p.err, 1u);
-    const long long b0 = c0 + (long long)warp * R;          // this warp's block of the chunk
-    const int rows_valid = ok ? (int)max(0LL, min((long long)R, c1 - b0)) : 0;
-    if (rows_valid > 0) {
+    const bool ok = mbar_wait_bounded(&full[stage], phase, abort_flag, p.err, 1u);
+    // the chunk's rows are dealt to the warps in blocks of R
+    for (long long b0 = c0 + (long long)warp * R; ok && b0 < c1; b0 += (long long)NW * R) {
+      const int rows_valid = (int)min((long long)R, c1 - b0);
       const unsigned char* st = smem + L.stage0 + (size_t)stage * L.stage_bytes;
       const int lr0 = (int)(b0 - t0);                       // block's first row within the stage
       const uint32_t* sK = reinterpret_cast<const uint32_t*>(st) + (size_t)lr0 * W;
@@ -357,18 +356,21 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       for (int g = 0; g < NG; ++g) pb[g] *= alpha;
 #pragma unroll
       for (int i = 0; i < NVL; ++i) {
+        float2* ps = reinterpret_cast<float2*>(sPS) + 2 * (rr[i] * PS_ROW + (my_h >> 1) * NG) + (my_h & 1);
         if (rr[i] < rows_valid) {
           const float pr = ex2(sc[i] - m_new);
           psum += pr;
           const float* av = sAV + rr[i] * NG;
           const float* bv = sBV + rr[i] * NG;
-          float2* ps = reinterpret_cast<float2*>(sPS) + 2 * (rr[i] * PS_ROW + (my_h >> 1) * NG) + (my_h & 1);
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
             const float x = pr * av[g];
             ps[2 * g] = make_float2(x, x);
             pb[g] = fmaf(pr, bv[g], pb[g]);
           }
+        } else {   // rows past the chunk take part in the V loop with weight 0
+#pragma unroll
+          for (int g = 0; g < NG; ++g) ps[2 * g] = make_float2(0.f, 0.f);
         }
       }
       l_run = fmaf(l_run, alpha, psum);
@@ -386,9 +388,8 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       const float4* psv = reinterpret_cast<const float4*>(sPS) + gv;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        if (r >= rows_valid) break;   // warp-uniform
         uint32_t w[VW];
-        load_words<VW>(sV + r * W + lane * VW, w);
+        load_words<VW>(sV + min(r, rows_valid - 1) * W + lane * VW, w);
         float2 f[EV / 2];
         unpack_words<BITS, EXACT, VW>(w, f);
         const float4* pr = psv + r * PS_ROW;
@@ -458,7 +459,10 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       }
       named_barrier_sync(1, NW * 32);
     }
-    ++i_chunk;
+    if (++stage == STAGES) {
+      stage = 0;
+      phase ^= 1;
+    }
   }
 }
 
