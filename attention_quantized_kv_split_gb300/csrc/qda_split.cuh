@@ -80,18 +80,56 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   }
 }
 
-// The producer warp: walks the CTA's chunks and fills the shared-memory ring. Per chunk: the K and V codes of its
-// rows and the 8-row aligned cover of its scales/biases (clipped to the arrays' end; a ragged last < 16 bytes go
-// by plain loads, published by the arrive), all completing on full[stage]. Lane 0 waits for the consumers to
-// free a stage (empty[stage]) and posts the byte count; lanes 0..5 then issue the six copies side by side. Before
-// returning, lane 0 waits until every copy the warp issued has landed. Called by all 32 lanes of the warp.
+// Fills ring slot `s` with one chunk [c0, c1) of the tile starting at row t0: the K and V codes of its rows and the
+// 8-row aligned cover of its scales/biases (clipped to the arrays' end; a ragged last < 16 bytes go by plain loads,
+// published by the arrive), all completing on full[s]. Lane 0 posts the byte count; lanes 0..5 then issue the six
+// copies side by side. Called by all 32 lanes of one warp.
+__device__ __forceinline__ void issue_chunk(const QdaParams& p, unsigned char* smem, const QdaSmemLayout& L,
+                                            uint64_t* full, int s, long long c0, long long c1, long long t0,
+                                            long long T, uint64_t pol) {
+  const int lane = threadIdx.x & 31;
+  const int NG = p.NG, W = p.W;
+  const uint32_t RB = W * 4, SB = NG * 2;
+  unsigned char* st = smem + L.stage0 + (size_t)s * L.stage_bytes;
+  const uint32_t cbytes = (uint32_t)(c1 - c0) * RB;
+  const size_t coff = (size_t)(c0 - t0) * RB;
+  const long long s0 = c0 & ~7LL;
+  const long long s1 = min((c1 + 7) & ~7LL, T);
+  const uint32_t sbytes = (uint32_t)(s1 - s0) * SB;
+  const uint32_t s16 = sbytes & ~15u;
+  const size_t soff = (size_t)(s0 - t0) * SB;
+  if (lane == 0) {
+    if (s16 != sbytes) {
+      const uint16_t* srcs[4] = {p.ks, p.kb, p.vs, p.vb};
+      for (int a = 0; a < 4; ++a) {
+        const uint16_t* src = srcs[a] + s0 * NG + s16 / 2;
+        uint16_t* dst = reinterpret_cast<uint16_t*>(st + 2 * L.codes_bytes + a * L.sc_bytes + soff + s16);
+        for (uint32_t k = 0; k < (sbytes - s16) / 2; ++k) dst[k] = src[k];
+      }
+    }
+    mbar_arrive_expect_tx(&full[s], 2 * cbytes + 4 * s16);
+  }
+  __syncwarp();
+  if (lane == 0) {
+    bulk_g2s(st + coff, p.kp + c0 * W, cbytes, &full[s], pol);
+  } else if (lane == 1) {
+    bulk_g2s(st + L.codes_bytes + coff, p.vp + c0 * W, cbytes, &full[s], pol);
+  } else if (lane < 6 && s16) {
+    const int a = lane - 2;
+    const uint16_t* src = a == 0 ? p.ks : a == 1 ? p.kb : a == 2 ? p.vs : p.vb;
+    bulk_g2s(st + 2 * L.codes_bytes + a * L.sc_bytes + soff, src + s0 * NG, s16, &full[s], pol);
+  }
+}
+
+// The producer warp: walks the CTA's chunks and fills the shared-memory ring. Lane 0 waits for the consumers to
+// free a stage (empty[stage]) before the chunk is issued into it. Before returning, lane 0 waits until every copy
+// the warp issued has landed. Called by all 32 lanes of the warp.
 __device__ __forceinline__ void produce_range(const QdaParams& p, ChunkWalker walk, unsigned char* smem,
                                               const QdaSmemLayout& L, uint64_t* full, uint64_t* empty,
                                               volatile int* abort_flag, long long T) {
   const int lane = threadIdx.x & 31;
-  const int STAGES = p.stages, NG = p.NG, W = p.W;
+  const int STAGES = p.stages;
   const uint64_t pol = policy_evict_first();
-  const uint32_t RB = W * 4, SB = NG * 2;
   long long c0, c1, t0;
   int i = 0;
   int s = 0, ph = 0;   // ring slot of chunk i and the parity of its use (i / STAGES) & 1
@@ -101,35 +139,7 @@ __device__ __forceinline__ void produce_range(const QdaParams& p, ChunkWalker wa
       if (lane == 0) ok = mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, p.err, 1u);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
     }
-    unsigned char* st = smem + L.stage0 + (size_t)s * L.stage_bytes;
-    const uint32_t cbytes = (uint32_t)(c1 - c0) * RB;
-    const size_t coff = (size_t)(c0 - t0) * RB;
-    const long long s0 = c0 & ~7LL;
-    const long long s1 = min((c1 + 7) & ~7LL, T);
-    const uint32_t sbytes = (uint32_t)(s1 - s0) * SB;
-    const uint32_t s16 = sbytes & ~15u;
-    const size_t soff = (size_t)(s0 - t0) * SB;
-    if (lane == 0) {
-      if (s16 != sbytes) {
-        const uint16_t* srcs[4] = {p.ks, p.kb, p.vs, p.vb};
-        for (int a = 0; a < 4; ++a) {
-          const uint16_t* src = srcs[a] + s0 * NG + s16 / 2;
-          uint16_t* dst = reinterpret_cast<uint16_t*>(st + 2 * L.codes_bytes + a * L.sc_bytes + soff + s16);
-          for (uint32_t k = 0; k < (sbytes - s16) / 2; ++k) dst[k] = src[k];
-        }
-      }
-      mbar_arrive_expect_tx(&full[s], 2 * cbytes + 4 * s16);
-    }
-    __syncwarp();
-    if (lane == 0) {
-      bulk_g2s(st + coff, p.kp + c0 * W, cbytes, &full[s], pol);
-    } else if (lane == 1) {
-      bulk_g2s(st + L.codes_bytes + coff, p.vp + c0 * W, cbytes, &full[s], pol);
-    } else if (lane < 6 && s16) {
-      const int a = lane - 2;
-      const uint16_t* src = a == 0 ? p.ks : a == 1 ? p.kb : a == 2 ? p.vs : p.vb;
-      bulk_g2s(st + 2 * L.codes_bytes + a * L.sc_bytes + soff, src + s0 * NG, s16, &full[s], pol);
-    }
+    issue_chunk(p, smem, L, full, s, c0, c1, t0, T, pol);
     ++i;
     if (++s == STAGES) {
       s = 0;

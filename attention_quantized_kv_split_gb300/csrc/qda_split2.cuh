@@ -279,13 +279,18 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       const uint16_t* sVS = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes + 2 * L.sc_bytes) + lr0 * NG;
       const uint16_t* sVB = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes + 3 * L.sc_bytes) + lr0 * NG;
 
-      // ---- phase 0: per-(row, group) coefficients of K and V
-      for (int idx = lane; idx < rows_valid * NG; idx += 32) {
-        const float2 ak = coeffs<BITS, EXACT_K>(half_bits_to_float_rt(sKS[idx], f16), half_bits_to_float_rt(sKB[idx], f16));
-        const float2 av = coeffs<BITS, EXACT>(half_bits_to_float_rt(sVS[idx], f16), half_bits_to_float_rt(sVB[idx], f16));
-        reinterpret_cast<float4*>(sAB)[idx] = make_float4(ak.x, ak.x, ak.y, ak.y);
-        sAV[idx] = av.x;
-        sBV[idx] = av.y;
+      // ---- phase 0: per-(row, group) coefficients of K and V (a fixed trip count, so all the loads issue at once)
+      constexpr int P0 = (R * NG + 31) / 32;
+#pragma unroll
+      for (int it = 0; it < P0; ++it) {
+        const int idx = lane + 32 * it;
+        if (idx < rows_valid * NG) {
+          const float2 ak = coeffs<BITS, EXACT_K>(half_bits_to_float_rt(sKS[idx], f16), half_bits_to_float_rt(sKB[idx], f16));
+          const float2 av = coeffs<BITS, EXACT>(half_bits_to_float_rt(sVS[idx], f16), half_bits_to_float_rt(sVB[idx], f16));
+          reinterpret_cast<float4*>(sAB)[idx] = make_float4(ak.x, ak.x, ak.y, ak.y);
+          sAV[idx] = av.x;
+          sBV[idx] = av.y;
+        }
       }
       __syncwarp();
 
@@ -301,18 +306,13 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
         const float4 ab = reinterpret_cast<const float4*>(sAB)[r * NG + gk];
 #pragma unroll
         for (int h = 0; h < NH; h += 2) {
-          // four independent chains of EK/4 packed FMAs (even and odd pairs of codes, two heads)
+          // one chain of EK/2 packed FMAs per head (the unrolled steps and heads give the ILP)
           float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-          float2 b0 = make_float2(0.f, 0.f), b1 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int k = 0; k < EK / 2; k += 2) {
+          for (int k = 0; k < EK / 2; ++k) {
             a0 = __ffma2_rn(f[k], qk[h][k], a0);
             a1 = __ffma2_rn(f[k], qk[h + 1][k], a1);
-            b0 = __ffma2_rn(f[k + 1], qk[h][k + 1], b0);
-            b1 = __ffma2_rn(f[k + 1], qk[h + 1][k + 1], b1);
           }
-          a0 = __fadd2_rn(a0, b0);
-          a1 = __fadd2_rn(a1, b1);
           const float2 sums = make_float2(a0.x + a0.y, a1.x + a1.y);
           const float2 part = __ffma2_rn(make_float2(ab.x, ab.y), sums,
                                          __fmul2_rn(make_float2(ab.z, ab.w), make_float2(qs[h], qs[h + 1])));
@@ -345,20 +345,27 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
         sc[i] = rr[i] < rows_valid ? v[i] : -INFINITY;
         bm = fmaxf(bm, sc[i]);
       }
+      // lazy rescaling: the reference max m_run of a head moves only when one of its scores exceeds it by more than
+      // 8 (a factor 2^8 in the weights), so most blocks skip the cross-lane max and the rescale; the partial keeps
+      // (m_run, sum, o) consistent whatever reference it ends with
+      const bool moved = __any_sync(0xffffffffu, bm > m_run + 8.f);
+      float alpha = 1.f;
+      if (moved) {
 #pragma unroll
-      for (int off = NH; off < 32; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
-      const float m_new = fmaxf(m_run, bm);
-      const float alpha = ex2(m_run - m_new);
-      const bool moved = __any_sync(0xffffffffu, m_new != m_run);
-      m_run = m_new;
+        for (int off = NH; off < 32; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+        const float m_new = fmaxf(m_run, bm);
+        alpha = ex2(m_run - m_new);
+        m_run = m_new;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) pb[g] *= alpha;
+        l_run *= alpha;
+      }
       float psum = 0.f;
-#pragma unroll
-      for (int g = 0; g < NG; ++g) pb[g] *= alpha;
 #pragma unroll
       for (int i = 0; i < NVL; ++i) {
         float2* ps = reinterpret_cast<float2*>(sPS) + 2 * (rr[i] * PS_ROW + (my_h >> 1) * NG) + (my_h & 1);
         if (rr[i] < rows_valid) {
-          const float pr = ex2(sc[i] - m_new);
+          const float pr = ex2(sc[i] - m_run);
           psum += pr;
           const float* av = sAV + rr[i] * NG;
           const float* bv = sBV + rr[i] * NG;
@@ -373,7 +380,7 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
           for (int g = 0; g < NG; ++g) ps[2 * g] = make_float2(0.f, 0.f);
         }
       }
-      l_run = fmaf(l_run, alpha, psum);
+      l_run += psum;
       __syncwarp();
 
       // ---- phase 4: V accumulation
