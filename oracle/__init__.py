@@ -9,6 +9,7 @@ from .qda_oracle import (  # noqa: F401
     attention_blocked,
     attention_head,
     attention_packed,
+    attention_packed_multi,
     bits16,
     dequantize,
     from_bits16,
@@ -19,4 +20,5 @@ from .qda_oracle import (  # noqa: F401
     seq_row_offsets,
     unit_rows,
     unpack,
+    visible_rows,
 )

@@ -19,6 +19,8 @@ What it computes, step by step, in the order of the method's description:
 5. ``attention_blocked``: the same result through per-block (max, sum-exp, unnormalised o) statistics and the
    merge ``out = sum_g o_g e^(m_g - M) / sum_g l_g e^(m_g - M)`` (``fused-decode-kernel.ts`` BLOCK_SOURCE and
    MERGE_SOURCE), used only to check that splitting the rows does not change the result.
+6. ``attention_packed_multi``: L query positions per sequence (the last L tokens, already in the cache), each
+   attending the rows up to its own (``visible_rows``); L = 1 is step 4.
 
 Readings taken where the pages are silent (each pinned by a test in ``tests/test_oracle.py``):
 
@@ -26,6 +28,8 @@ Readings taken where the pages are silent (each pinned by a test in ``tests/test
 * a code is ``clamp(rint((x - b_hat) / s_hat), 0, 2^bits - 1)`` with every operation in IEEE fp32 and
   round-half-to-even; a group whose stored scale is 0 gets code 0;
 * the attention itself is exact fp64 on the dequantized values; no intermediate is rounded to bf16/fp16.
+* with L query positions per sequence, position l attends the first N - L + 1 + l rows (causal among the L
+  new tokens, which are the last L rows of the cache).
 
 Layouts match the GPU library's: q ``[B, H, D]``; per sequence b (back to back, no padding) the packed cache is
 ``[Hkv, N[b], D*bits/32]`` uint32 and the scales and biases ``[Hkv, N[b], D/GS]``.
@@ -213,6 +217,49 @@ def attention_packed(q, kp, ks, kb, vp, vs, vb, N, H: int, Hkv: int, D: int, GS:
             cache = {key: (Kd, Vd)}          # keep one unit resident: bounded memory at large N
         Kd, Vd = cache[key]
         res[(b, h)] = attention_head(q[b, h], Kd, Vd)
+    return res
+
+
+def visible_rows(n: int, L: int, l: int) -> int:
+    """Rows of a sequence of ``n`` cache rows that query position ``l`` of ``L`` attends.
+
+    The L query positions are the sequence's last L tokens, whose K and V rows are already in the cache (rows
+    n - L .. n - 1); position l sees every row up to and including its own, ``n - L + 1 + l`` rows in all. With
+    L = 1 this is the whole window of single-query decode (mlx-bun ``fused-decode-kernel.ts``, header comment:
+    L > 1 goes to a separate N-tiled path; @mlx-bun/inference ``trellis/reduce.ts``: matrix-vector kernels take
+    up to ``TRELLIS_MATVEC_MAX_M = 4`` rows at once).
+    """
+    if not 1 <= L <= n or not 0 <= l < L:
+        raise ValueError("need 1 <= L <= n and 0 <= l < L")
+    return n - L + 1 + l
+
+
+def attention_packed_multi(q, kp, ks, kb, vp, vs, vb, N, L: int, H: int, Hkv: int, D: int, GS: int, bits: int,
+                           heads=None):
+    """Decode attention for L query positions per sequence from the packed cache (small-L multi-query decode).
+
+    q ``[B, L, H, D]`` (values); cache arrays as in ``attention_packed``. Query (b, l, h) attends the first
+    ``visible_rows(N[b], L, l)`` rows of its KV head ``h // (H / Hkv)``. ``heads``: iterable of (b, l, h)
+    (default all). Returns {(b, l, h): out[D] fp64}.
+    """
+    q = np.asarray(q, np.float64)
+    B = len(N)
+    nrep = H // Hkv
+    if heads is None:
+        heads = [(b, l, h) for b in range(B) for l in range(L) for h in range(H)]
+    res = {}
+    cache = {}
+    for b, l, h in heads:
+        kvh = h // nrep
+        key = (b, kvh)
+        if key not in cache:
+            r0, r1 = unit_rows(N, Hkv, b, kvh)
+            Kd = dequantize(unpack(kp[r0:r1], bits, D), ks[r0:r1], kb[r0:r1], GS)
+            Vd = dequantize(unpack(vp[r0:r1], bits, D), vs[r0:r1], vb[r0:r1], GS)
+            cache = {key: (Kd, Vd)}
+        Kd, Vd = cache[key]
+        n = visible_rows(int(N[b]), L, l)
+        res[(b, l, h)] = attention_head(q[b, l, h], Kd[:n], Vd[:n])
     return res
 
 

@@ -286,3 +286,71 @@ def test_packed_interface_ragged_layout():
             np.testing.assert_array_equal(got[(b, h)], ref[h])
         r += Hkv * n
     assert r == rows
+
+
+# ----------------------------------------------------------------------- small-L multi-query decode (L queries)
+
+
+def test_visible_rows_closed_form():
+    # the L new tokens are the last L cache rows; position l sees rows 0 .. n - L + l
+    assert [O.visible_rows(10, 3, l) for l in range(3)] == [8, 9, 10]
+    assert O.visible_rows(5, 1, 0) == 5
+    assert [O.visible_rows(4, 4, l) for l in range(4)] == [1, 2, 3, 4]
+    for bad in ((3, 4, 0), (5, 2, 2), (5, 0, 0), (5, 2, -1)):
+        with pytest.raises(ValueError):
+            O.visible_rows(*bad)
+
+
+def _multi_case(seed, N, L, H, Hkv, D, GS, bits, dtype="bf16"):
+    rng = np.random.default_rng(seed)
+    rows = Hkv * sum(N)
+    Kx = rng.standard_normal((rows, D)).astype(np.float32)
+    Vx = rng.standard_normal((rows, D)).astype(np.float32)
+    cache = O.quantize_cache(Kx, Vx, GS, bits, dtype)
+    q = O.round_to(rng.standard_normal((len(N), L, H, D)).astype(np.float32), dtype).astype(np.float64)
+    return q, cache, Kx, Vx
+
+
+def test_multi_query_matches_masked_sdpa():
+    # library routine with an explicit causal mask over the whole window, instead of truncating the rows
+    N, L, H, Hkv, D, GS, bits = [6, 9], 3, 4, 2, 32, 32, 4
+    q, cache, _, _ = _multi_case(21, N, L, H, Hkv, D, GS, bits)
+    got = O.attention_packed_multi(q, *cache, N, L, H, Hkv, D, GS, bits)
+    kp, ks, kb, vp, vs, vb = cache
+    nrep = H // Hkv
+    for b, n in enumerate(N):
+        mask = torch.tensor([[k <= n - L + l for k in range(n)] for l in range(L)])
+        for h in range(H):
+            r0, r1 = O.unit_rows(N, Hkv, b, h // nrep)
+            K = torch.from_numpy(O.dequantize(O.unpack(kp[r0:r1], bits, D), ks[r0:r1], kb[r0:r1], GS))
+            V = torch.from_numpy(O.dequantize(O.unpack(vp[r0:r1], bits, D), vs[r0:r1], vb[r0:r1], GS))
+            ref = torch.nn.functional.scaled_dot_product_attention(torch.from_numpy(q[b, :, h]), K, V, attn_mask=mask)
+            for l in range(L):
+                np.testing.assert_allclose(got[(b, l, h)], ref[l].numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_multi_query_last_position_is_single_query():
+    # the last position sees the whole window: single-query decode over the same cache
+    N, L, H, Hkv, D, GS, bits = [5, 12], 4, 8, 2, 64, 32, 8
+    q, cache, _, _ = _multi_case(22, N, L, H, Hkv, D, GS, bits, "fp16")
+    got = O.attention_packed_multi(q, *cache, N, L, H, Hkv, D, GS, bits)
+    ref = O.attention_packed(q[:, L - 1], *cache, N, H, Hkv, D, GS, bits)
+    for b in range(len(N)):
+        for h in range(H):
+            np.testing.assert_array_equal(got[(b, L - 1, h)], ref[(b, h)])
+
+
+def test_multi_query_ignores_rows_after_own_position():
+    # changing row n - L + l + 1 of a unit changes what position l + 1 sees but not position l
+    N, L, H, Hkv, D, GS, bits = [10], 3, 2, 1, 32, 32, 4
+    q, cache, Kx, Vx = _multi_case(23, N, L, H, Hkv, D, GS, bits)
+    base = O.attention_packed_multi(q, *cache, N, L, H, Hkv, D, GS, bits)
+    for l in range(L - 1):
+        row = N[0] - L + l + 1
+        K2, V2 = Kx.copy(), Vx.copy()
+        K2[row] *= -3.0
+        V2[row] += 5.0
+        alt = O.attention_packed_multi(q, *O.quantize_cache(K2, V2, GS, bits, "bf16"), N, L, H, Hkv, D, GS, bits)
+        for h in range(H):
+            np.testing.assert_array_equal(alt[(0, l, h)], base[(0, l, h)])
+            assert np.abs(alt[(0, l + 1, h)] - base[(0, l + 1, h)]).max() > 1e-3
