@@ -66,6 +66,20 @@ def qdecode_attn_noalloc(q: torch.Tensor, k_packed: torch.Tensor, k_scales: torc
     return out
 
 
+def qdecode_attn_multi(q: torch.Tensor, k_packed: torch.Tensor, k_scales: torch.Tensor, k_biases: torch.Tensor,
+                       v_packed: torch.Tensor, v_scales: torch.Tensor, v_biases: torch.Tensor, out: torch.Tensor,
+                       N: Sequence[int], Hkv: int, GS: int, bits: int, stream=None) -> torch.Tensor:
+    """Small-L multi-query decode: q and out ``[B, L, H, D]``; the L positions are each sequence's last L tokens
+    (already the last L rows of its cache, counted in N), and position l attends the first N[b] - L + 1 + l
+    rows. Cache arguments as for qdecode_attn."""
+    B, L, H, D = q.shape
+    st = lib().qdecode_attn_multi(_ptr(q), _ptr(k_packed), _ptr(k_scales), _ptr(k_biases), _ptr(v_packed),
+                                  _ptr(v_scales), _ptr(v_biases), _ptr(out), B, L, H, Hkv, _lib.int32_array(N), D,
+                                  GS, bits, dtype_code(q.dtype, out.dtype), _stream(stream))
+    _lib.check(st, "qdecode_attn_multi")
+    return out
+
+
 def bind_qdecode_attn(q: torch.Tensor, k_packed: torch.Tensor, k_scales: torch.Tensor, k_biases: torch.Tensor,
                       v_packed: torch.Tensor, v_scales: torch.Tensor, v_biases: torch.Tensor, out: torch.Tensor,
                       N: Sequence[int], Hkv: int, GS: int, bits: int, stream=None):
@@ -91,6 +105,15 @@ def qdecode_attn_plan(B: int, H: int, Hkv: int, N: Sequence[int], D: int, GS: in
     st = lib().qdecode_attn_plan(B, H, Hkv, _lib.int32_array(N), D, GS, bits, num_sms, ctas_per_sm,
                                  ctypes.byref(plan))
     _lib.check(st, "qdecode_attn_plan")
+    return plan.as_dict()
+
+
+def qdecode_attn_multi_plan(B: int, L: int, H: int, Hkv: int, N: Sequence[int], D: int, GS: int, bits: int,
+                            num_sms: int = 0, ctas_per_sm: int = 0) -> dict:
+    plan = QdaPlan()
+    st = lib().qdecode_attn_multi_plan(B, L, H, Hkv, _lib.int32_array(N), D, GS, bits, num_sms, ctas_per_sm,
+                                       ctypes.byref(plan))
+    _lib.check(st, "qdecode_attn_multi_plan")
     return plan.as_dict()
 
 

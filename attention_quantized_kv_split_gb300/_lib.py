@@ -19,6 +19,7 @@ QDA_STATIC_SCRATCH_BYTES = 8 << 20
 QDA_BF16, QDA_FP16, QDA_FP32 = 1, 2, 3
 QDA_MAX_B = 512
 QDA_MAX_NREP = 64
+QDA_MAX_L = 8
 
 
 class QdaPlan(ctypes.Structure):
@@ -46,6 +47,8 @@ _PI32 = ctypes.POINTER(ctypes.c_int32)
 SIGNATURES = {
     "qdecode_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _PI32, _I, _I, _I, _I, _P]),
     "qdecode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _PI32, _I, _I, _I, _I, _P]),
+    "qdecode_attn_multi": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _PI32, _I, _I, _I, _I, _P]),
+    "qdecode_attn_multi_plan": (_I, [_I, _I, _I, _I, _PI32, _I, _I, _I, _I, _I, ctypes.POINTER(QdaPlan)]),
     "qdecode_attn_plan": (_I, [_I, _I, _I, _PI32, _I, _I, _I, _I, _I, ctypes.POINTER(QdaPlan)]),
     "qdecode_attn_workspace_bytes": (_I, [_I, _I, _I, _PI32, _I, _I, _I, ctypes.POINTER(_SZ)]),
     "qdecode_attn_set_workspace": (_I, [_P, _SZ]),

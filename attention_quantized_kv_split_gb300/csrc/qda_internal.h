@@ -13,7 +13,7 @@
 
 // Launch parameters of the split and merge kernels (passed by value as a __grid_constant__).
 struct QdaParams {
-  const void* q;              // [B, H, D] input dtype
+  const void* q;              // [B, L, H, D] input dtype
   const uint32_t* kp;         // packed K codes, rows of W words
   const uint16_t* ks;         // K scales, rows of NG 16-bit values
   const uint16_t* kb;         // K biases
@@ -25,11 +25,20 @@ struct QdaParams {
   unsigned int* err;          // device error word
   long long total_rows;       // T = Hkv * sum(N)
   int B, H, Hkv, D, GS, NG, W, nrep, heads_pad, head_chunks, num_ctas, tile_rows, stages;
+  int L;                      // query positions per sequence; head j of a KV head is (position j / nrep, j % nrep)
   int tile_shift;             // log2(tile_rows): pipeline tiles are powers of two
   int f16;                    // q / scales / biases are fp16 (else bf16)
   float qscale;               // log2(e) / sqrt(D): scores come out in log2 units
   int seq_off[QDA_MAX_B + 1]; // seq_off[b] = N[0] + ... + N[b-1]
 };
+
+// Query head j (0 <= j < nrep * L) of KV head kvh of sequence b: its row of q / out ([B, L, H, D] as rows of D)
+// and how many of the unit's last rows it must not see (the L new tokens are causal among themselves).
+__host__ __device__ inline long long qda_q_row(int b, int kvh, int j, int nrep, int L, int H) {
+  const int l = j / nrep;
+  return ((long long)b * L + l) * H + (long long)kvh * nrep + (j - l * nrep);
+}
+__host__ __device__ inline int qda_hidden_tail(int j, int nrep, int L) { return L - 1 - j / nrep; }
 
 // Row range of CTA c: [qda_cta_row(c), qda_cta_row(c + 1)). Interior boundaries are multiples of 8 rows so that
 // every scale/bias tile a CTA copies starts on a 16-byte boundary whatever the group count per row.

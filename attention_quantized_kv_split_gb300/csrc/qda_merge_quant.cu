@@ -32,8 +32,10 @@ __device__ __forceinline__ void store4(void* out, size_t idx, float4 v) {
   }
 }
 
-// out[b, h, :] = sum_s o_s 2^(m_s - M) / sum_s l_s 2^(m_s - M) over the partial slots of (b, KV head of h)
-// (mlx-bun fused-decode-kernel.ts, MERGE_SOURCE), in log2 units. One CTA per (b, h). The slots are dealt to
+// out[b, l, h, :] = sum_s o_s 2^(m_s - M) / sum_s l_s 2^(m_s - M) over the partial slots of (b, KV head of h)
+// (mlx-bun fused-decode-kernel.ts, MERGE_SOURCE), in log2 units. One CTA per (b, l, h); l is the query position
+// (always 0 for single-query decode). A slot whose rows were all hidden from the head holds m = -inf and is
+// skipped. The slots are dealt to
 // kMergeThreads / (D/4) thread groups round-robin; each thread folds its slots in one pass with a running max, so
 // the (m, l) and o loads of a slot are issued together, and the groups are then combined in a fixed order:
 // deterministic, no atomics.
@@ -46,9 +48,10 @@ __global__ void __launch_bounds__(kMergeThreads) qda_merge_kernel(const __grid_c
   __shared__ float2 red_ml[kMergeThreads];
   const int tid = threadIdx.x;
   const int D = p.D;
-  const int bh = blockIdx.x;
-  const int b = bh / p.H, h = bh - b * p.H;
-  const int kvh = h / p.nrep, j = h - kvh * p.nrep;
+  const int bh = blockIdx.x;   // (b * L + l) * H + h: also the output row
+  const int bl = bh / p.H, h = bh - bl * p.H;
+  const int b = bl / p.L, l = bl - b * p.L;
+  const int kvh = h / p.nrep, j = l * p.nrep + (h - kvh * p.nrep);
   const int unit = b * p.Hkv + kvh;
   const long long n = p.seq_off[b + 1] - p.seq_off[b];
   const long long us = (long long)p.Hkv * p.seq_off[b] + (long long)kvh * n;
@@ -72,9 +75,12 @@ __global__ void __launch_bounds__(kMergeThreads) qda_merge_kernel(const __grid_c
     const float2 ml = p.part_ml[hp];
     const float4 v = reinterpret_cast<const float4*>(p.part_o + hp * D)[t];
     if (maybe_empty && qda_cta_row(T, C, c) == qda_cta_row(T, C, c + 1)) continue;
-    const float mn = fmaxf(m_run, ml.x);
+    // a slot whose rows were all hidden from this query position holds (m, l, o) = (-inf, 0, 0): taken as a
+    // finite m it adds nothing and never forms -inf - -inf
+    const float mx = fmaxf(ml.x, -1e30f);
+    const float mn = fmaxf(m_run, mx);
     const float a = ex2m(m_run - mn);   // 0 on the first slot
-    const float w = ex2m(ml.x - mn);
+    const float w = ex2m(mx - mn);
     den = fmaf(den, a, ml.y * w);
     acc.x = fmaf(acc.x, a, v.x * w);
     acc.y = fmaf(acc.y, a, v.y * w);
@@ -218,7 +224,7 @@ cudaError_t launch_quant(const float* x, long long rows, int D, int GS, uint32_t
 
 cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.B * p.H));
+  cfg.gridDim = dim3((unsigned)(p.B * p.L * p.H));
   cfg.blockDim = dim3(qda::kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;

@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
   const int rir = lane / LPR;     // row of the warp step this lane works on
   const int lir = lane % LPR;     // lane's slice of the row: elements [lir*E, lir*E + E)
   float qv[NH][E], qsum[NH], o[NH][E], m[NH], l[NH];
+  int hide[NH];   // last rows of the unit each head must not see (multi-query decode)
   int cur_unit = -1;
   int s = 0, phase = 0;   // ring slot of the current chunk and the parity of its use
   while (walk.next(p, c0, c1, t0)) {
@@ -214,9 +215,10 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
       for (int h = 0; h < NH; ++h) {
         const int j = hc * NH + h;
         float acc = 0.f;
-        if (j < p.nrep) {
+        hide[h] = qda_hidden_tail(j, p.nrep, p.L);
+        if (j < p.nrep * p.L) {
           const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
-                               ((size_t)walk.b * p.H + (size_t)walk.kvh * p.nrep + j) * D + lir * E;
+                               qda_q_row(walk.b, walk.kvh, j, p.nrep, p.L, p.H) * D + lir * E;
 #pragma unroll
           for (int e = 0; e < E; ++e) {
             qv[h][e] = half_bits_to_float_rt(qp[e], f16) * p.qscale;
@@ -275,7 +277,8 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
         float pr[NH], alpha[NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
-          const float sh = valid ? sc[h] : -INFINITY;
+          const bool seen = valid && row < walk.u_end - hide[h];
+          const float sh = seen ? sc[h] : -INFINITY;
           float mx = sh;
 #pragma unroll
           for (int off = LPR; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -285,7 +288,7 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
             pr[h] = 0.f;
           } else {
             alpha[h] = ex2(m[h] - mn);
-            pr[h] = valid ? ex2(sh - mn) : 0.f;
+            pr[h] = seen ? ex2(sh - mn) : 0.f;
           }
           m[h] = mn;
           l[h] = fmaf(l[h], alpha[h], pr[h]);

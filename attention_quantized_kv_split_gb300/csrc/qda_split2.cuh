@@ -136,7 +136,8 @@ struct Split2Geom {
   static_assert(NVL >= 1, "reduction must end with at least one score per lane");
 };
 
-template <int BITS, int D, int NH, int NG, bool EXACT>
+// MULTI: L > 1 query positions per sequence, so the last L - 1 rows of a unit are hidden from some heads.
+template <int BITS, int D, int NH, int NG, bool EXACT, bool MULTI>
 __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid_constant__ QdaParams p) {
   using G = Split2Geom<BITS, D, NH>;
   constexpr int EK = G::EK, LK = G::LK, RPS = G::RPS, R = G::R, S = G::S, NV = G::NV, NVL = G::NVL;
@@ -227,6 +228,7 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
   float qs[NH];             // its sum (bias term)
   float2 o[NH][EV / 2];     // V accumulators
   float m_run = -INFINITY;  // running max of my head (equal across the lanes owning it)
+  int my_hide = 0;          // last rows of the unit my head must not see (MULTI)
   float l_run = 0.f;        // sum of 2^(s - m_run) over my rows
   float pb[NG];             // sum of p * B_v per group, my head
   int cur_unit = -1;
@@ -239,9 +241,9 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       for (int h = 0; h < NH; ++h) {
         const int j = hc * NH + h;
         float acc = 0.f;
-        if (j < p.nrep) {
+        if (j < p.nrep * p.L) {
           const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
-                               ((size_t)walk.b * p.H + (size_t)walk.kvh * p.nrep + j) * D + klane * EK;
+                               qda_q_row(walk.b, walk.kvh, j, p.nrep, p.L, p.H) * D + klane * EK;
           const uint4 a = reinterpret_cast<const uint4*>(qp)[0];
           const uint4 b = reinterpret_cast<const uint4*>(qp)[1];
           const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -262,6 +264,7 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       }
       m_run = -INFINITY;
       l_run = 0.f;
+      if constexpr (MULTI) my_hide = qda_hidden_tail(hc * NH + my_h, p.nrep, p.L);
 #pragma unroll
       for (int g = 0; g < NG; ++g) pb[g] = 0.f;
     }
@@ -335,14 +338,19 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
         }
       }
 
-      // ---- phase 3: block softmax for my head over my rows
+      // ---- phase 3: block softmax for my head over my rows (the first `seen` rows of the block are visible to it)
+      int seen = rows_valid;
+      if constexpr (MULTI) {
+        const long long vis = walk.u_end - my_hide - b0;
+        seen = vis < rows_valid ? (int)max(vis, 0LL) : rows_valid;
+      }
       float sc[NVL];
       int rr[NVL];
       float bm = -INFINITY;
 #pragma unroll
       for (int i = 0; i < NVL; ++i) {
         rr[i] = my_s[i] * RPS + khalf;
-        sc[i] = rr[i] < rows_valid ? v[i] : -INFINITY;
+        sc[i] = rr[i] < seen ? v[i] : -INFINITY;
         bm = fmaxf(bm, sc[i]);
       }
       // lazy rescaling: the reference max m_run of a head moves only when one of its scores exceeds it by more than
@@ -354,7 +362,11 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
 #pragma unroll
         for (int off = NH; off < 32; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
         const float m_new = fmaxf(m_run, bm);
-        alpha = ex2(m_run - m_new);
+        if constexpr (MULTI) {
+          alpha = m_new == -INFINITY ? 1.f : ex2(m_run - m_new);   // a head with nothing visible yet keeps 0
+        } else {
+          alpha = ex2(m_run - m_new);
+        }
         m_run = m_new;
 #pragma unroll
         for (int g = 0; g < NG; ++g) pb[g] *= alpha;
@@ -364,7 +376,7 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
 #pragma unroll
       for (int i = 0; i < NVL; ++i) {
         float2* ps = reinterpret_cast<float2*>(sPS) + 2 * (rr[i] * PS_ROW + (my_h >> 1) * NG) + (my_h & 1);
-        if (rr[i] < rows_valid) {
+        if (rr[i] < seen) {
           const float pr = ex2(sc[i] - m_run);
           psum += pr;
           const float* av = sAV + rr[i] * NG;
@@ -375,7 +387,7 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
             ps[2 * g] = make_float2(x, x);
             pb[g] = fmaf(pr, bv[g], pb[g]);
           }
-        } else {   // rows past the chunk take part in the V loop with weight 0
+        } else {   // rows past the chunk (or hidden from the head) take part in the V loop with weight 0
 #pragma unroll
           for (int g = 0; g < NG; ++g) ps[2 * g] = make_float2(0.f, 0.f);
         }
@@ -473,10 +485,10 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
   }
 }
 
-template <int BITS, bool EXACT, typename Fn>
-cudaError_t with_split2_kernel(int D, int nh, int ng, Fn&& f) {
+template <int BITS, bool EXACT, bool MULTI, typename Fn>
+cudaError_t with_split2_kernel_m(int D, int nh, int ng, Fn&& f) {
 #define QDA_V2(D_, NH_, NG_) \
-  if (D == D_ && nh == NH_ && ng == NG_) return f(qda_split2_kernel<BITS, D_, NH_, NG_, EXACT>);
+  if (D == D_ && nh == NH_ && ng == NG_) return f(qda_split2_kernel<BITS, D_, NH_, NG_, EXACT, MULTI>);
   QDA_V2(256, 2, 2) QDA_V2(256, 2, 4) QDA_V2(256, 2, 8)
   QDA_V2(256, 4, 2) QDA_V2(256, 4, 4) QDA_V2(256, 4, 8)
   QDA_V2(512, 2, 4) QDA_V2(512, 2, 8) QDA_V2(512, 2, 16)
@@ -484,9 +496,15 @@ cudaError_t with_split2_kernel(int D, int nh, int ng, Fn&& f) {
   return cudaErrorInvalidValue;
 }
 
+template <int BITS, bool EXACT, typename Fn>
+cudaError_t with_split2_kernel(int D, int nh, int ng, bool multi, Fn&& f) {
+  return multi ? with_split2_kernel_m<BITS, EXACT, true>(D, nh, ng, f)
+               : with_split2_kernel_m<BITS, EXACT, false>(D, nh, ng, f);
+}
+
 template <int BITS, bool EXACT>
 cudaError_t launch_split2(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem, cudaStream_t s) {
-  return with_split2_kernel<BITS, EXACT>(D, nh, ng, [&](auto kern) -> cudaError_t {
+  return with_split2_kernel<BITS, EXACT>(D, nh, ng, p.L > 1, [&](auto kern) -> cudaError_t {
     cudaError_t e = ensure_smem_limit(kern, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, QDA_THREADS, smem, s>>>(p);
@@ -496,7 +514,8 @@ cudaError_t launch_split2(const QdaParams& p, int D, int nh, int ng, dim3 grid, 
 
 template <int BITS, bool EXACT>
 cudaError_t occupancy_split2(int D, int nh, int ng, size_t smem, int* n) {
-  return with_split2_kernel<BITS, EXACT>(D, nh, ng, [&](auto kern) -> cudaError_t {
+  // both instances of a shape have the same resources; the single-query one stands for both
+  return with_split2_kernel<BITS, EXACT>(D, nh, ng, false, [&](auto kern) -> cudaError_t {
     cudaError_t e = ensure_smem_limit(kern, smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, QDA_THREADS, smem);

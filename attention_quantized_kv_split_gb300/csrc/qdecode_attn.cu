@@ -50,19 +50,20 @@ int pow2ceil(int x) {
 }
 
 // Pure host checks of the shape (no pointers): the support predicate of mlx-bun fused-decode-kernel.ts
-// (fusedDecodeKernelSupported), widened to B >= 1 sequences, any H % Hkv == 0 and fp16 or bf16 input.
-int check_shape(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits) {
+// (fusedDecodeKernelSupported), widened to B >= 1 sequences, any H % Hkv == 0, fp16 or bf16 input and L query
+// positions per sequence.
+int check_shape(int B, int L, int H, int Hkv, const int32_t* N, int D, int GS, int bits) {
   if (N == nullptr) return QDA_ERR_INVALID;
-  if (B < 1 || H < 1 || Hkv < 1 || D < 1 || GS < 1) return QDA_ERR_INVALID;
+  if (B < 1 || L < 1 || H < 1 || Hkv < 1 || D < 1 || GS < 1) return QDA_ERR_INVALID;
   if (H % Hkv != 0) return QDA_ERR_INVALID;
   for (int b = 0; b < B && b <= QDA_MAX_B; ++b)
-    if (N[b] < 1) return QDA_ERR_INVALID;
+    if (N[b] < L) return QDA_ERR_INVALID;
   if (bits != 4 && bits != 8) return QDA_ERR_UNSUPPORTED;
   if (GS != 32 && GS != 64 && GS != 128) return QDA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128 && D != 256 && D != 512) return QDA_ERR_UNSUPPORTED;
   if (D % GS != 0) return QDA_ERR_UNSUPPORTED;
   if (B > QDA_MAX_B) return QDA_ERR_UNSUPPORTED;
-  if (H / Hkv > QDA_MAX_NREP) return QDA_ERR_UNSUPPORTED;
+  if (L > QDA_MAX_L || (H / Hkv) * L > QDA_MAX_NREP) return QDA_ERR_UNSUPPORTED;
   long long total = 0;
   for (int b = 0; b < B; ++b) total += N[b];
   if (total > (1LL << 31) - 1) return QDA_ERR_UNSUPPORTED;   // sequence offsets are int32
@@ -90,11 +91,11 @@ constexpr size_t kSmemBudget = 112 * 1024;   // two CTAs per SM
 // Rows per warp block of the lean kernel (its Split2Geom<...>::R).
 int split2_rows(int D, int nh) { return nh == 4 ? 8 : 16; }
 
-Variant pick_variant(int H, int Hkv, int D, int GS, int bits) {
+// nrep: query heads served per KV head (H / Hkv, times L for multi-query decode).
+Variant pick_variant(int nrep, int D, int GS, int bits) {
   Variant v;
   v.W = D * bits / 32;
   v.NG = D / GS;
-  const int nrep = H / Hkv;
   const size_t row_bytes = 2 * (size_t)v.W * 4 + 4 * (size_t)v.NG * 2;
   if (D == 256 || D == 512) {
     v.kind = 2;
@@ -157,8 +158,8 @@ cudaError_t split_launch(int bits, bool exact, const QdaParams& p, const Variant
 
 // The plan: one contiguous, equal share of the flattened rows per CTA, as many CTAs as fit on the GPU at once
 // (one wave), but no fewer than kMinRowsPerCta rows each. Deterministic in (shape, SM count, occupancy).
-void make_plan(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int num_sms, int ctas_per_sm,
-               const Variant& v, qda_plan* plan) {
+void make_plan(int B, int Hkv, const int32_t* N, int D, int num_sms, int ctas_per_sm, const Variant& v,
+               qda_plan* plan) {
   long long sumN = 0;
   for (int b = 0; b < B; ++b) sumN += N[b];
   const long long T = (long long)Hkv * sumN;
@@ -182,8 +183,6 @@ void make_plan(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits,
   const size_t o_bytes = (size_t)plan->slots * v.heads_pad * D * sizeof(float);
   const size_t ml_bytes = (size_t)plan->slots * v.heads_pad * 2 * sizeof(float);
   plan->workspace_bytes = ((o_bytes + 255) & ~(size_t)255) + ml_bytes;
-  (void)GS;
-  (void)bits;
 }
 
 DeviceState* device_state(int* dev_out) {
@@ -223,16 +222,20 @@ int occupancy_for(DeviceState& d, int bits, int D, bool exact, const Variant& v,
   return QDA_OK;
 }
 
-}  // namespace
+// ------------------------------------------------------------------------------------------------------------
+// Scratch of the allocation-free entry point: its partial results live in this fixed device array instead of a
+// cudaMalloc'ed workspace. Host code must not pass the array's name to a kernel (on the host it names a stand-in, not device
+// memory): the device address is looked up once per device with cudaGetSymbolAddress and cached.
+static __device__ __align__(256) unsigned char g_qda_static_scratch[QDA_STATIC_SCRATCH_BYTES];
+std::mutex g_static_mu;
+void* g_static_scratch_addr[kMaxDevices] = {};
 
-extern "C" {
-
-int qdecode_attn_plan(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int num_sms,
-                      int ctas_per_sm, qda_plan* plan) {
+int plan_impl(int B, int L, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int num_sms, int ctas_per_sm,
+              qda_plan* plan) {
   if (plan == nullptr) return QDA_ERR_INVALID;
-  int st = check_shape(B, H, Hkv, N, D, GS, bits);
+  int st = check_shape(B, L, H, Hkv, N, D, GS, bits);
   if (st != QDA_OK) return st;
-  const Variant v = pick_variant(H, Hkv, D, GS, bits);
+  const Variant v = pick_variant((H / Hkv) * L, D, GS, bits);
   if (num_sms <= 0 || ctas_per_sm <= 0) {
     int dev;
     DeviceState* d = device_state(&dev);
@@ -244,69 +247,52 @@ int qdecode_attn_plan(int B, int H, int Hkv, const int32_t* N, int D, int GS, in
       if (st != QDA_OK) return st;
     }
   }
-  make_plan(B, H, Hkv, N, D, GS, bits, num_sms, ctas_per_sm, v, plan);
+  make_plan(B, Hkv, N, D, num_sms, ctas_per_sm, v, plan);
   return QDA_OK;
 }
 
-int qdecode_attn_workspace_bytes(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, size_t* bytes) {
-  if (bytes == nullptr) return QDA_ERR_INVALID;
-  qda_plan plan;
-  const int st = qdecode_attn_plan(B, H, Hkv, N, D, GS, bits, 0, 0, &plan);
-  if (st != QDA_OK) return st;
-  *bytes = plan.workspace_bytes;
-  return QDA_OK;
-}
+// Where a call's partial results live.
+enum class Scratch { kWorkspace, kStatic };
 
-int qdecode_attn_set_workspace(void* ptr, size_t bytes) {
-  if (ptr != nullptr && !aligned16(ptr)) return QDA_ERR_ALIGN;
-  int dev;
-  DeviceState* d = device_state(&dev);
-  if (d == nullptr) return QDA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(d->mu);
-  d->user_ws = ptr;
-  d->user_ws_bytes = ptr ? bytes : 0;
-  return QDA_OK;
-}
-
-int qdecode_attn_debug_force_splits(int num_ctas) {
-  if (num_ctas < 0) return QDA_ERR_INVALID;
-  g_force_splits.store(num_ctas);
-  return QDA_OK;
-}
-
-int qdecode_attn_set_split_event(void* event) {
-  t_split_event = event;
-  return QDA_OK;
-}
-
-int qdecode_attn(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
-                 const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out, int B, int H,
-                 int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream) {
+// Every decode entry point: checks, plan, scratch, parameters, the split and merge launches.
+int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
+             const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out, int B, int L, int H,
+             int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream, Scratch where) {
   if (!q || !k_packed || !k_scales || !k_biases || !v_packed || !v_scales || !v_biases || !out)
     return QDA_ERR_INVALID;
   int in_dt, out_dt;
   int st = check_dtype(dtype, &in_dt, &out_dt);
   if (st != QDA_OK) return st;
-  st = check_shape(B, H, Hkv, N, D, GS, bits);
+  st = check_shape(B, L, H, Hkv, N, D, GS, bits);
   if (st != QDA_OK) return st;
   const void* ptrs[8] = {q, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, out};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return QDA_ERR_ALIGN;
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return QDA_ERR_ALIGN;
 
   int dev;
   DeviceState* d = device_state(&dev);
   if (d == nullptr) return QDA_ERR_CUDA;
-  const bool f16 = in_dt == QDA_FP16;
-  const Variant v = pick_variant(H, Hkv, D, GS, bits);
-  int occ = 1;
+  const int nrep = H / Hkv;
+  const Variant v = pick_variant(nrep * L, D, GS, bits);
   const bool exact = out_dt == QDA_FP32;
+  int occ = 1;
   st = occupancy_for(*d, bits, D, exact, v, &occ);
   if (st != QDA_OK) return st;
   qda_plan plan;
-  make_plan(B, H, Hkv, N, D, GS, bits, d->num_sms, occ, v, &plan);
+  make_plan(B, Hkv, N, D, d->num_sms, occ, v, &plan);
 
   void* ws = nullptr;
-  {
+  if (where == Scratch::kStatic) {
+    if (plan.workspace_bytes > (size_t)QDA_STATIC_SCRATCH_BYTES) return QDA_ERR_SCRATCH;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_scratch_addr[dev] == nullptr) {
+      void* ptr = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&ptr, g_qda_static_scratch);
+      if (e != cudaSuccess) return cuda_fail(e);
+      g_static_scratch_addr[dev] = ptr;
+    }
+    ws = g_static_scratch_addr[dev];
+  } else {
     std::lock_guard<std::mutex> lock(d->mu);
     if (d->user_ws != nullptr) {
       if (d->user_ws_bytes < plan.workspace_bytes) return QDA_ERR_WORKSPACE;
@@ -340,13 +326,14 @@ int qdecode_attn(const void* q, const uint32_t* k_packed, const void* k_scales, 
   p.err = d->err;
   p.total_rows = plan.total_rows;
   p.B = B;
+  p.L = L;
   p.H = H;
   p.Hkv = Hkv;
   p.D = D;
   p.GS = GS;
   p.NG = v.NG;
   p.W = v.W;
-  p.nrep = H / Hkv;
+  p.nrep = nrep;
   p.heads_pad = v.heads_pad;
   p.head_chunks = v.hc;
   p.num_ctas = plan.num_ctas;
@@ -354,7 +341,7 @@ int qdecode_attn(const void* q, const uint32_t* k_packed, const void* k_scales, 
   p.stages = v.stages;
   p.tile_shift = 0;
   while ((1 << p.tile_shift) < v.tile) ++p.tile_shift;
-  p.f16 = f16 ? 1 : 0;
+  p.f16 = in_dt == QDA_FP16 ? 1 : 0;
   p.qscale = 1.4426950408889634f / sqrtf((float)D);
   p.seq_off[0] = 0;
   for (int b = 0; b < B; ++b) p.seq_off[b + 1] = p.seq_off[b] + N[b];
@@ -362,7 +349,7 @@ int qdecode_attn(const void* q, const uint32_t* k_packed, const void* k_scales, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = split_launch(bits, exact, p, v, dim3((unsigned)plan.num_ctas * (unsigned)v.hc), s);
   if (e != cudaSuccess) return cuda_fail(e);
-  const bool use_event = t_split_event != nullptr;
+  const bool use_event = t_split_event != nullptr && where == Scratch::kWorkspace;
   if (use_event) {
     e = cudaEventRecord(static_cast<cudaEvent_t>(t_split_event), s);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -371,6 +358,73 @@ int qdecode_attn(const void* q, const uint32_t* k_packed, const void* k_scales, 
   if (e != cudaSuccess) return cuda_fail(e);
   g_calls.fetch_add(1);
   return QDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qdecode_attn_plan(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int num_sms,
+                      int ctas_per_sm, qda_plan* plan) {
+  return plan_impl(B, 1, H, Hkv, N, D, GS, bits, num_sms, ctas_per_sm, plan);
+}
+
+int qdecode_attn_multi_plan(int B, int L, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int num_sms,
+                            int ctas_per_sm, qda_plan* plan) {
+  return plan_impl(B, L, H, Hkv, N, D, GS, bits, num_sms, ctas_per_sm, plan);
+}
+
+int qdecode_attn_workspace_bytes(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, size_t* bytes) {
+  if (bytes == nullptr) return QDA_ERR_INVALID;
+  qda_plan plan;
+  const int st = plan_impl(B, 1, H, Hkv, N, D, GS, bits, 0, 0, &plan);
+  if (st != QDA_OK) return st;
+  *bytes = plan.workspace_bytes;
+  return QDA_OK;
+}
+
+int qdecode_attn_set_workspace(void* ptr, size_t bytes) {
+  if (ptr != nullptr && !aligned16(ptr)) return QDA_ERR_ALIGN;
+  int dev;
+  DeviceState* d = device_state(&dev);
+  if (d == nullptr) return QDA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(d->mu);
+  d->user_ws = ptr;
+  d->user_ws_bytes = ptr ? bytes : 0;
+  return QDA_OK;
+}
+
+int qdecode_attn_debug_force_splits(int num_ctas) {
+  if (num_ctas < 0) return QDA_ERR_INVALID;
+  g_force_splits.store(num_ctas);
+  return QDA_OK;
+}
+
+int qdecode_attn_set_split_event(void* event) {
+  t_split_event = event;
+  return QDA_OK;
+}
+
+int qdecode_attn(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
+                 const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out, int B, int H,
+                 int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream) {
+  return run_call(q, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, out, B, 1, H, Hkv, N, D, GS, bits,
+                  dtype, stream, Scratch::kWorkspace);
+}
+
+int qdecode_attn_multi(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
+                       const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out, int B, int L,
+                       int H, int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream) {
+  return run_call(q, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, out, B, L, H, Hkv, N, D, GS, bits,
+                  dtype, stream, Scratch::kWorkspace);
+}
+
+// The allocation-free entry point: partial results in the fixed device array above, never in an allocation.
+int qdecode_attn_noalloc(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
+                         const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out, int B,
+                         int H, int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream) {
+  return run_call(q, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, out, B, 1, H, Hkv, N, D, GS, bits,
+                  dtype, stream, Scratch::kStatic);
 }
 
 int qdecode_quantize(const float* x, long long rows, int D, int GS, int bits, int dtype, uint32_t* packed,
@@ -426,95 +480,3 @@ int qdecode_attn_device_status(unsigned int* flags) {
 long long qdecode_attn_calls(void) { return g_calls.load(); }
 
 }  // extern "C"
-
-// ------------------------------------------------------------------------------------------------------------
-// Allocation-free entry point. Its partial results live in this fixed device array instead of a cudaMalloc'ed
-// workspace. Host code must not pass the array's name to a kernel (on the host it names a stand-in, not device
-// memory): the device address is looked up once per device with cudaGetSymbolAddress and cached.
-namespace {
-static __device__ __align__(256) unsigned char g_qda_static_scratch[QDA_STATIC_SCRATCH_BYTES];
-std::mutex g_static_mu;
-void* g_static_scratch_addr[kMaxDevices] = {};
-}  // namespace
-
-extern "C" int qdecode_attn_noalloc(const void* q, const uint32_t* k_packed, const void* k_scales,
-                                    const void* k_biases, const uint32_t* v_packed, const void* v_scales,
-                                    const void* v_biases, void* out, int B, int H, int Hkv, const int32_t* N,
-                                    int D, int GS, int bits, int dtype, void* stream) {
-  if (!q || !k_packed || !k_scales || !k_biases || !v_packed || !v_scales || !v_biases || !out)
-    return QDA_ERR_INVALID;
-  int in_dt, out_dt;
-  int st = check_dtype(dtype, &in_dt, &out_dt);
-  if (st != QDA_OK) return st;
-  st = check_shape(B, H, Hkv, N, D, GS, bits);
-  if (st != QDA_OK) return st;
-  const void* ptrs[8] = {q, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, out};
-  for (const void* ptr : ptrs)
-    if (!aligned16(ptr)) return QDA_ERR_ALIGN;
-
-  int dev;
-  DeviceState* d = device_state(&dev);
-  if (d == nullptr) return QDA_ERR_CUDA;
-  const Variant v = pick_variant(H, Hkv, D, GS, bits);
-  const bool exact = out_dt == QDA_FP32;
-  int occ = 1;
-  st = occupancy_for(*d, bits, D, exact, v, &occ);
-  if (st != QDA_OK) return st;
-  qda_plan plan;
-  make_plan(B, H, Hkv, N, D, GS, bits, d->num_sms, occ, v, &plan);
-  if (plan.workspace_bytes > (size_t)QDA_STATIC_SCRATCH_BYTES) return QDA_ERR_SCRATCH;
-
-  void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_static_mu);
-    if (g_static_scratch_addr[dev] == nullptr) {
-      void* ptr = nullptr;
-      cudaError_t e = cudaGetSymbolAddress(&ptr, g_qda_static_scratch);
-      if (e != cudaSuccess) return cuda_fail(e);
-      g_static_scratch_addr[dev] = ptr;
-    }
-    scratch = g_static_scratch_addr[dev];
-  }
-
-  QdaParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.q = q;
-  p.kp = k_packed;
-  p.ks = static_cast<const uint16_t*>(k_scales);
-  p.kb = static_cast<const uint16_t*>(k_biases);
-  p.vp = v_packed;
-  p.vs = static_cast<const uint16_t*>(v_scales);
-  p.vb = static_cast<const uint16_t*>(v_biases);
-  const size_t o_bytes = (size_t)plan.slots * v.heads_pad * D * sizeof(float);
-  p.part_o = static_cast<float*>(scratch);
-  p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(scratch) + ((o_bytes + 255) & ~(size_t)255));
-  p.err = d->err;
-  p.total_rows = plan.total_rows;
-  p.B = B;
-  p.H = H;
-  p.Hkv = Hkv;
-  p.D = D;
-  p.GS = GS;
-  p.NG = v.NG;
-  p.W = v.W;
-  p.nrep = H / Hkv;
-  p.heads_pad = v.heads_pad;
-  p.head_chunks = v.hc;
-  p.num_ctas = plan.num_ctas;
-  p.tile_rows = v.tile;
-  p.stages = v.stages;
-  p.tile_shift = 0;
-  while ((1 << p.tile_shift) < v.tile) ++p.tile_shift;
-  p.f16 = in_dt == QDA_FP16 ? 1 : 0;
-  p.qscale = 1.4426950408889634f / sqrtf((float)D);
-  p.seq_off[0] = 0;
-  for (int b = 0; b < B; ++b) p.seq_off[b + 1] = p.seq_off[b] + N[b];
-
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = split_launch(bits, exact, p, v, dim3((unsigned)plan.num_ctas * (unsigned)v.hc), s);
-  if (e != cudaSuccess) return cuda_fail(e);
-  e = qda_launch_merge(p, out, out_dt, true, s);
-  if (e != cudaSuccess) return cuda_fail(e);
-  g_calls.fetch_add(1);
-  return QDA_OK;
-}

@@ -82,7 +82,7 @@ def _gen(seed: int, *key: int, device="cpu") -> torch.Generator:
     return g
 
 
-T_Q, T_K, T_V, T_LEN, T_OUTL, T_PLANT_ROWS, T_PLANT_DIR = range(1, 8)
+T_Q, T_K, T_V, T_LEN, T_OUTL, T_PLANT_ROWS, T_PLANT_DIR, T_QMULTI = range(1, 9)
 
 
 def lengths(w: Workload) -> List[int]:
@@ -98,6 +98,13 @@ def query(w: Workload, device="cpu") -> torch.Tensor:
     """q ``[B, H, D]`` ~ N(0, 1), rounded to the input dtype."""
     g = _gen(w.seed, T_Q, device=device)
     q = torch.randn(w.B, w.H, w.D, generator=g, device=device, dtype=torch.float32)
+    return q.to(DT[w.dtype_in])
+
+
+def query_multi(w: Workload, L: int, device="cpu") -> torch.Tensor:
+    """q ``[B, L, H, D]`` ~ N(0, 1) for L query positions per sequence, rounded to the input dtype."""
+    g = _gen(w.seed, T_QMULTI, L, device=device)
+    q = torch.randn(w.B, L, w.H, w.D, generator=g, device=device, dtype=torch.float32)
     return q.to(DT[w.dtype_in])
 
 

@@ -44,9 +44,10 @@ extern "C" {
 #endif
 
 #define QDA_OK 0
-#define QDA_ERR_INVALID (-1)     /* null pointer, non-positive size, H % Hkv != 0, N[b] < 1, bad dtype code */
+#define QDA_ERR_INVALID (-1)     /* null pointer, non-positive size, H % Hkv != 0, N[b] < 1 (N[b] < L for
+                                    qdecode_attn_multi), bad dtype code */
 #define QDA_ERR_UNSUPPORTED (-2) /* bits not in {4, 8}, GS not in {32, 64, 128}, D not in {64, 128, 256, 512},
-                                    D % GS != 0, B > QDA_MAX_B, H / Hkv > QDA_MAX_NREP */
+                                    D % GS != 0, B > QDA_MAX_B, L * H / Hkv > QDA_MAX_NREP, L > QDA_MAX_L */
 #define QDA_ERR_ALIGN (-3)       /* a data pointer is not 16-byte aligned */
 #define QDA_ERR_CUDA (-4)        /* CUDA runtime error; see qdecode_attn_last_cuda_error() */
 #define QDA_ERR_WORKSPACE (-5)   /* the caller-provided workspace is smaller than the call needs */
@@ -61,6 +62,7 @@ extern "C" {
 
 #define QDA_MAX_B 512
 #define QDA_MAX_NREP 64
+#define QDA_MAX_L 8
 
 /*
  * qdecode_attn: decode attention for B sequences (the operation above). Asynchronous on `stream` (a
@@ -95,11 +97,32 @@ int qdecode_attn_noalloc(const void* q, const uint32_t* k_packed, const void* k_
                          const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out,
                          int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream);
 
+/*
+ * qdecode_attn_multi: small-L multi-query decode (for example verifying L speculative tokens). Each sequence b
+ * has L query positions, its last L tokens, whose K and V rows are already the last L rows of its cache (N[b]
+ * counts them, so N[b] >= L). Query position l (0 <= l < L) attends the rows up to and including its own, the
+ * first N[b] - L + 1 + l rows of its KV head:
+ *
+ *     out[b, l, h, :] = sum_{n < N[b]-L+1+l} softmax_n( q[b, l, h, :] . k_hat[b, kv, n, :] / sqrt(D) ) v_hat[b, kv, n, :]
+ *
+ * (The single-query kernel of mlx-bun fused-decode-kernel.ts leaves L > 1 to a separate path, header comment; the
+ * matrix-vector kernels of @mlx-bun/inference trellis/reduce.ts take up to TRELLIS_MATVEC_MAX_M = 4 rows.) The L
+ * positions of a KV head's query heads share one stream of its cache rows: every (position, head) pair is served
+ * like one more query head of the KV head. q and out are [B, L, H, D]; everything else (cache layout, dtype,
+ * workspace, stream, errors) is as for qdecode_attn, and L = 1 gives qdecode_attn's result bit for bit.
+ * Requires 1 <= L <= QDA_MAX_L and L * (H / Hkv) <= QDA_MAX_NREP (else QDA_ERR_UNSUPPORTED; L < 1 or N[b] < L is
+ * QDA_ERR_INVALID). Its plan and workspace size come from qdecode_attn_multi_plan.
+ */
+int qdecode_attn_multi(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
+                       const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out,
+                       int B, int L, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int dtype,
+                       void* stream);
+
 /* The launch plan qdecode_attn would use (host only). Determined by the shape and the GPU alone. */
 typedef struct {
   int num_ctas;           /* CTAs along the flattened row space (each takes one contiguous row range) */
-  int head_chunks;        /* CTAs per row range when one CTA cannot hold all H/Hkv query heads of a KV head */
-  int heads_per_cta;      /* query heads a CTA serves (H/Hkv rounded up to a power of two, capped) */
+  int head_chunks;        /* CTAs per row range when one CTA cannot hold all L*H/Hkv query heads of a KV head */
+  int heads_per_cta;      /* query heads (position, head pairs when L > 1) a CTA serves */
   int tile_rows;          /* cache rows per pipeline stage */
   int stages;             /* pipeline depth (stages of tile_rows rows in flight per CTA) */
   int threads;            /* threads per CTA */
@@ -116,6 +139,10 @@ typedef struct {
  */
 int qdecode_attn_plan(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int num_sms,
                       int ctas_per_sm, qda_plan* plan);
+
+/* qdecode_attn_plan for L query positions per sequence (the plan qdecode_attn_multi uses); L = 1 is the same. */
+int qdecode_attn_multi_plan(int B, int L, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int num_sms,
+                            int ctas_per_sm, qda_plan* plan);
 
 /* Workspace size in bytes qdecode_attn needs for this shape on the current device. */
 int qdecode_attn_workspace_bytes(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, size_t* bytes);

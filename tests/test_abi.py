@@ -168,3 +168,62 @@ def test_plan_argument_errors(L):
     assert L.qdecode_attn_plan(1, 8, 2, _lib.int32_array([4]), 256, 64, 4, 152, 2, None) == _lib.QDA_ERR_INVALID
     assert L.qdecode_attn_plan(1, 8, 3, _lib.int32_array([4]), 256, 64, 4, 152, 2, ctypes.byref(p)) == -1
     assert L.qdecode_attn_plan(1, 8, 2, _lib.int32_array([4]), 256, 64, 5, 152, 2, ctypes.byref(p)) == -2
+
+
+def call_multi(L, B=1, Lq=2, H=8, Hkv=2, N=(512,), D=256, GS=64, bits=4, dtype=1):
+    p = [FAKE + 256 * i for i in range(8)]
+    return L.qdecode_attn_multi(*p, B, Lq, H, Hkv, _lib.int32_array(N), D, GS, bits, dtype, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Lq=0), _lib.QDA_ERR_INVALID),
+    (dict(Lq=-1), _lib.QDA_ERR_INVALID),
+    (dict(Lq=_lib.QDA_MAX_L + 1, N=(64,)), _lib.QDA_ERR_UNSUPPORTED),
+    (dict(Lq=4, N=(3,)), _lib.QDA_ERR_INVALID),              # fewer cache rows than query positions
+    (dict(B=2, Lq=3, N=(9, 2)), _lib.QDA_ERR_INVALID),
+    (dict(Lq=8, H=64, Hkv=4, N=(64,)), _lib.QDA_ERR_UNSUPPORTED),   # 8 positions x 16 heads > QDA_MAX_NREP
+    (dict(bits=3), _lib.QDA_ERR_UNSUPPORTED),
+    (dict(H=6, Hkv=4), _lib.QDA_ERR_INVALID),
+])
+def test_multi_argument_errors(L, kw, status):
+    assert call_multi(L, **kw) == status
+
+
+def test_multi_pointer_checks(L):
+    p = [FAKE + 256 * i for i in range(8)]
+    p[3] = None
+    assert L.qdecode_attn_multi(*p, 1, 2, 8, 2, _lib.int32_array([64]), 256, 64, 4, 1, None) == _lib.QDA_ERR_INVALID
+    p = [FAKE + 256 * i for i in range(8)]
+    p[7] += 2
+    assert L.qdecode_attn_multi(*p, 1, 2, 8, 2, _lib.int32_array([64]), 256, 64, 4, 1, None) == _lib.QDA_ERR_ALIGN
+
+
+def multi_plan(L, B, Lq, H, Hkv, N, D, GS, bits, sms=152, occ=2):
+    p = _lib.QdaPlan()
+    st = L.qdecode_attn_multi_plan(B, Lq, H, Hkv, _lib.int32_array(N), D, GS, bits, sms, occ, ctypes.byref(p))
+    assert st == 0
+    return p.as_dict()
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 8, 2, [512], 256, 64, 4),
+    (1, 16, 8, [8192], 256, 32, 8),
+    (1, 16, 8, [32768], 512, 128, 4),
+    (3, 24, 3, [5, 7, 9], 128, 32, 8),
+])
+@pytest.mark.parametrize("Lq", [1, 2, 3, 4, 8])
+def test_multi_plan_serves_every_position(L, shape, Lq):
+    B, H, Hkv, N, D, GS, bits = shape
+    if Lq > min(N):   # a sequence shorter than its query positions
+        st = L.qdecode_attn_multi_plan(B, Lq, H, Hkv, _lib.int32_array(N), D, GS, bits, 152, 2,
+                                       ctypes.byref(_lib.QdaPlan()))
+        assert st == _lib.QDA_ERR_INVALID
+        return
+    p = multi_plan(L, B, Lq, H, Hkv, N, D, GS, bits)
+    assert p["heads_per_cta"] * p["head_chunks"] >= (H // Hkv) * Lq
+    assert p["total_rows"] == Hkv * sum(N) and p["slots"] == p["num_ctas"] + B * Hkv
+    assert p["smem_bytes"] <= 227 * 1024 and p["stages"] >= 2
+    hp = p["heads_per_cta"] * p["head_chunks"]
+    assert p["workspace_bytes"] >= p["slots"] * hp * (D + 2) * 4
+    if Lq == 1:
+        assert p == plan(L, *shape)
