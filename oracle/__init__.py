@@ -7,6 +7,9 @@ from .qda_oracle import (  # noqa: F401
     DTYPES,
     attention,
     attention_blocked,
+    attention_head_compat,
+    attention_packed_compat,
+    attention_two_pass_blocked,
     attention_head,
     attention_packed,
     attention_packed_multi,

@@ -21,13 +21,16 @@ What it computes, step by step, in the order of the method's description:
    MERGE_SOURCE), used only to check that splitting the rows does not change the result.
 6. ``attention_packed_multi``: L query positions per sequence (the last L tokens, already in the cache), each
    attending the rows up to its own (``visible_rows``); L = 1 is step 4.
+7. ``attention_head_compat`` / ``attention_two_pass_blocked`` / ``attention_packed_compat``: the two-pass variant
+   with the pages' compat rounding points (scores and normalised probabilities rounded to the input dtype T).
 
 Readings taken where the pages are silent (each pinned by a test in ``tests/test_oracle.py``):
 
 * the scale and bias are computed in fp32 from fp32 data and stored rounded (RNE) to the q dtype (bf16 or fp16);
 * a code is ``clamp(rint((x - b_hat) / s_hat), 0, 2^bits - 1)`` with every operation in IEEE fp32 and
   round-half-to-even; a group whose stored scale is 0 gets code 0;
-* the attention itself is exact fp64 on the dequantized values; no intermediate is rounded to bf16/fp16.
+* the attention itself is exact fp64 on the dequantized values; no intermediate is rounded to bf16/fp16
+  (except in the compat form of step 7, which rounds where the pages' two-pass kernels do);
 * with L query positions per sequence, position l attends the first N - L + 1 + l rows (causal among the L
   new tokens, which are the last L rows of the cache).
 
@@ -175,6 +178,47 @@ def attention_blocked(q, K, V, S: int) -> np.ndarray:
     return num / den
 
 
+def attention_head_compat(q, K, V, dtype: str) -> np.ndarray:
+    """One head in the pages' two-pass form with its rounding points (mlx-bun ``fused-decode-kernel.ts`` header:
+    kernel A takes per-block (max, sum-exp) over scores rounded to T, kernel C sums ``T(exp(s - M) / denom) *
+    dequant(V)`` with the full-row (M, denom), the merge sums the blocks and casts to T).
+
+    T is ``dtype`` (bf16 or fp16). A score is ``q . k / sqrt(D)``, rounded to fp32 and then to T (the two steps a
+    fp32 kernel takes); a probability is ``exp(s - M) / denom`` in fp64, rounded to fp32 and then to T; the
+    weighted V sum is fp64 and is not renormalised. The caller rounds the output to its dtype.
+    """
+    q = np.asarray(q, np.float64)
+    K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64)
+    D = q.shape[-1]
+    s = round_to(((K @ q) / math.sqrt(D)).astype(np.float32), dtype).astype(np.float64)
+    M = s.max()
+    e = np.exp(s - M)
+    p = round_to((e / e.sum()).astype(np.float32), dtype).astype(np.float64)
+    return p @ V
+
+
+def attention_two_pass_blocked(q, K, V, S: int, dtype: str) -> np.ndarray:
+    """``attention_head_compat`` computed as the pages' two passes over S contiguous blocks: per-block (m, l) of the
+    rounded scores, the full-row (M, denom) from them, per-block sums of rounded probabilities times V, and the
+    blocks added in order."""
+    q = np.asarray(q, np.float64)
+    N = K.shape[0]
+    D = q.shape[-1]
+    edges = [(N * i) // S for i in range(S + 1)]
+    blocks = [(a, b) for a, b in zip(edges[:-1], edges[1:]) if b > a]
+    score = [round_to(((np.asarray(K[a:b], np.float64) @ q) / math.sqrt(D)).astype(np.float32), dtype)
+             .astype(np.float64) for a, b in blocks]
+    stats = [(s.max(), np.exp(s - s.max()).sum()) for s in score]            # pass A
+    M = max(m for m, _ in stats)
+    denom = sum(l * math.exp(m - M) for m, l in stats)
+    out = np.zeros(V.shape[-1])
+    for (a, b), s in zip(blocks, score):                                        # pass B, then the sum
+        p = round_to((np.exp(s - M) / denom).astype(np.float32), dtype).astype(np.float64)
+        out = out + p @ np.asarray(V[a:b], np.float64)
+    return out
+
+
 # ------------------------------------------------------------------------------- the packed-cache interface
 
 
@@ -260,6 +304,29 @@ def attention_packed_multi(q, kp, ks, kb, vp, vs, vb, N, L: int, H: int, Hkv: in
         Kd, Vd = cache[key]
         n = visible_rows(int(N[b]), L, l)
         res[(b, l, h)] = attention_head(q[b, l, h], Kd[:n], Vd[:n])
+    return res
+
+
+def attention_packed_compat(q, kp, ks, kb, vp, vs, vb, N, H: int, Hkv: int, D: int, GS: int, bits: int,
+                            dtype: str, heads=None):
+    """``attention_packed`` with the two-pass rounding points of ``attention_head_compat`` (T = ``dtype``)."""
+    q = np.asarray(q, np.float64)
+    B = len(N)
+    nrep = H // Hkv
+    if heads is None:
+        heads = [(b, h) for b in range(B) for h in range(H)]
+    res = {}
+    cache = {}
+    for b, h in heads:
+        kvh = h // nrep
+        key = (b, kvh)
+        if key not in cache:
+            r0, r1 = unit_rows(N, Hkv, b, kvh)
+            Kd = dequantize(unpack(kp[r0:r1], bits, D), ks[r0:r1], kb[r0:r1], GS)
+            Vd = dequantize(unpack(vp[r0:r1], bits, D), vs[r0:r1], vb[r0:r1], GS)
+            cache = {key: (Kd, Vd)}
+        Kd, Vd = cache[key]
+        res[(b, h)] = attention_head_compat(q[b, h], Kd, Vd, dtype)
     return res
 
 

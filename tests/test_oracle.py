@@ -354,3 +354,82 @@ def test_multi_query_ignores_rows_after_own_position():
         for h in range(H):
             np.testing.assert_array_equal(alt[(0, l, h)], base[(0, l, h)])
             assert np.abs(alt[(0, l + 1, h)] - base[(0, l + 1, h)]).max() > 1e-3
+
+
+# ------------------------------------------------------------------ two-pass variant with compat rounding points
+
+
+@pytest.mark.parametrize("dtype,third", [("bf16", 0.333984375), ("fp16", 0.333251953125)])
+def test_compat_equal_scores_weights_are_rounded_thirds(dtype, third):
+    # three equal scores: each probability is T(1/3) (not renormalised), so o = T(1/3) * (v0 + v1 + v2)
+    rng = np.random.default_rng(31)
+    D = 64
+    K = np.tile(rng.standard_normal(D), (3, 1))
+    V = rng.standard_normal((3, D))
+    q = rng.standard_normal(D)
+    out = O.attention_head_compat(q, K, V, dtype)
+    np.testing.assert_allclose(out, third * V.sum(0), rtol=1e-15, atol=1e-15)
+
+
+def test_compat_scores_round_before_the_softmax():
+    # scores 1 and 1 + 2^-10 are one value in bf16 (ulp 2^-7 at 1): equal weights 1/2, unlike the exact softmax;
+    # in fp16 (ulp 2^-10 at 1) they stay apart
+    D = 64
+    q = np.zeros(D)
+    q[0] = 8.0                                  # sqrt(D): score = K[:, 0]
+    K = np.zeros((2, D))
+    K[0, 0], K[1, 0] = 1.0, 1.0 + 2.0 ** -10
+    V = np.zeros((2, D))
+    V[0, 1], V[1, 1] = 1.0, -1.0
+    assert O.attention_head_compat(q, K, V, "bf16")[1] == 0.0
+    w = math.exp(2.0 ** -10)
+    p0, p1 = O.round_to(np.array([1 / (1 + w), w / (1 + w)], np.float32), "fp16").astype(np.float64)
+    assert O.attention_head_compat(q, K, V, "fp16")[1] == p0 - p1 != 0.0
+    assert abs(O.attention_head(q, K, V)[1] - (1 - w) / (1 + w)) < 1e-15
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_compat_matches_library_softmax_with_casts(dtype):
+    # the same rounding points through torch: fp64 scores cast to fp32 then T, torch.softmax, cast, matmul
+    rng = np.random.default_rng(32)
+    N, D = 50, 128
+    q = rng.standard_normal(D)
+    K = rng.standard_normal((N, D))
+    V = rng.standard_normal((N, D))
+    T = {"bf16": torch.bfloat16, "fp16": torch.float16}[dtype]
+    s = (torch.from_numpy(K) @ torch.from_numpy(q) / math.sqrt(D)).float().to(T).double()
+    p = torch.softmax(s, 0).float().to(T).double()
+    ref = (p @ torch.from_numpy(V)).numpy()
+    np.testing.assert_allclose(O.attention_head_compat(q, K, V, dtype), ref, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 7, 40])
+def test_two_pass_blocked_equals_direct(S):
+    rng = np.random.default_rng(33 + S)
+    N, D = 40, 64
+    q = rng.standard_normal(D) * 2
+    K = rng.standard_normal((N, D))
+    V = rng.standard_normal((N, D))
+    for dtype in ("bf16", "fp16"):
+        ref = O.attention_head_compat(q, K, V, dtype)
+        blk = O.attention_two_pass_blocked(q, K, V, S, dtype)
+        assert np.abs(blk - ref).max() <= 1e-12 * np.abs(ref).max()
+
+
+def test_compat_packed_interface():
+    rng = np.random.default_rng(34)
+    N = [4, 9]
+    B, H, Hkv, D, GS, bits = 2, 4, 2, 64, 32, 4
+    rows = Hkv * sum(N)
+    Kx = rng.standard_normal((rows, D)).astype(np.float32)
+    Vx = rng.standard_normal((rows, D)).astype(np.float32)
+    cache = O.quantize_cache(Kx, Vx, GS, bits, "bf16")
+    q = rng.standard_normal((B, H, D))
+    got = O.attention_packed_compat(q, *cache, N, H, Hkv, D, GS, bits, "bf16")
+    kp, ks, kb, vp, vs, vb = cache
+    for b in range(B):
+        for h in range(H):
+            r0, r1 = O.unit_rows(N, Hkv, b, h // 2)
+            K = O.dequantize(O.unpack(kp[r0:r1], bits, D), ks[r0:r1], kb[r0:r1], GS)
+            V = O.dequantize(O.unpack(vp[r0:r1], bits, D), vs[r0:r1], vb[r0:r1], GS)
+            np.testing.assert_array_equal(got[(b, h)], O.attention_head_compat(q[b, h], K, V, "bf16"))
