@@ -26,6 +26,9 @@ struct QdaParams {
   long long total_rows;       // T = Hkv * sum(N)
   int B, H, Hkv, D, GS, NG, W, nrep, heads_pad, head_chunks, num_ctas, tile_rows, stages;
   int L;                      // query positions per sequence; head j of a KV head is (position j / nrep, j % nrep)
+  int mode;                   // lean split kernel: 0 single-pass, 1 multi-query, 2 compat pass A, 3 compat pass B
+  int k_only;                 // the ring carries K only (compat pass A)
+  int compat;                 // merge: plain sum of the partials (compat pass B wrote normalised sums)
   int tile_shift;             // log2(tile_rows): pipeline tiles are powers of two
   int f16;                    // q / scales / biases are fp16 (else bf16)
   float qscale;               // log2(e) / sqrt(D): scores come out in log2 units

@@ -35,7 +35,8 @@ __device__ __forceinline__ void store4(void* out, size_t idx, float4 v) {
 // out[b, l, h, :] = sum_s o_s 2^(m_s - M) / sum_s l_s 2^(m_s - M) over the partial slots of (b, KV head of h)
 // (mlx-bun fused-decode-kernel.ts, MERGE_SOURCE), in log2 units. One CTA per (b, l, h); l is the query position
 // (always 0 for single-query decode). A slot whose rows were all hidden from the head holds m = -inf and is
-// skipped. The slots are dealt to
+// skipped. In compat mode (the two-pass form) the partials already carry normalised weights and are only summed
+// (in the same fixed order): out = T(sum_s o_s). The slots are dealt to
 // kMergeThreads / (D/4) thread groups round-robin; each thread folds its slots in one pass with a running max, so
 // the (m, l) and o loads of a slot are issued together, and the groups are then combined in a fixed order:
 // deterministic, no atomics.
@@ -77,11 +78,11 @@ __global__ void __launch_bounds__(kMergeThreads) qda_merge_kernel(const __grid_c
     if (maybe_empty && qda_cta_row(T, C, c) == qda_cta_row(T, C, c + 1)) continue;
     // a slot whose rows were all hidden from this query position holds (m, l, o) = (-inf, 0, 0): taken as a
     // finite m it adds nothing and never forms -inf - -inf
-    const float mx = fmaxf(ml.x, -1e30f);
+    const float mx = p.compat ? 0.f : fmaxf(ml.x, -1e30f);   // compat: every slot weighs 1
     const float mn = fmaxf(m_run, mx);
     const float a = ex2m(m_run - mn);   // 0 on the first slot
     const float w = ex2m(mx - mn);
-    den = fmaf(den, a, ml.y * w);
+    den = fmaf(den, a, (p.compat ? 0.f : ml.y) * w);
     acc.x = fmaf(acc.x, a, v.x * w);
     acc.y = fmaf(acc.y, a, v.y * w);
     acc.z = fmaf(acc.z, a, v.z * w);
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(kMergeThreads) qda_merge_kernel(const __grid_c
     o.z = fmaf(v.z, w, o.z);
     o.w = fmaf(v.w, w, o.w);
   }
-  const float inv = 1.0f / dt;
+  const float inv = p.compat ? 1.f : 1.0f / dt;
   o.x *= inv;
   o.y *= inv;
   o.z *= inv;

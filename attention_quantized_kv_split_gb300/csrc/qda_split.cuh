@@ -98,23 +98,24 @@ __device__ __forceinline__ void issue_chunk(const QdaParams& p, unsigned char* s
   const uint32_t sbytes = (uint32_t)(s1 - s0) * SB;
   const uint32_t s16 = sbytes & ~15u;
   const size_t soff = (size_t)(s0 - t0) * SB;
+  const int arrays = p.k_only ? 2 : 4;   // scale/bias arrays copied: K's, and V's unless the ring carries K only
   if (lane == 0) {
     if (s16 != sbytes) {
       const uint16_t* srcs[4] = {p.ks, p.kb, p.vs, p.vb};
-      for (int a = 0; a < 4; ++a) {
+      for (int a = 0; a < arrays; ++a) {
         const uint16_t* src = srcs[a] + s0 * NG + s16 / 2;
         uint16_t* dst = reinterpret_cast<uint16_t*>(st + 2 * L.codes_bytes + a * L.sc_bytes + soff + s16);
         for (uint32_t k = 0; k < (sbytes - s16) / 2; ++k) dst[k] = src[k];
       }
     }
-    mbar_arrive_expect_tx(&full[s], 2 * cbytes + 4 * s16);
+    mbar_arrive_expect_tx(&full[s], (p.k_only ? 1 : 2) * cbytes + arrays * s16);
   }
   __syncwarp();
   if (lane == 0) {
     bulk_g2s(st + coff, p.kp + c0 * W, cbytes, &full[s], pol);
   } else if (lane == 1) {
-    bulk_g2s(st + L.codes_bytes + coff, p.vp + c0 * W, cbytes, &full[s], pol);
-  } else if (lane < 6 && s16) {
+    if (!p.k_only) bulk_g2s(st + L.codes_bytes + coff, p.vp + c0 * W, cbytes, &full[s], pol);
+  } else if (lane < 2 + arrays && s16) {
     const int a = lane - 2;
     const uint16_t* src = a == 0 ? p.ks : a == 1 ? p.kb : a == 2 ? p.vs : p.vb;
     bulk_g2s(st + 2 * L.codes_bytes + a * L.sc_bytes + soff, src + s0 * NG, s16, &full[s], pol);

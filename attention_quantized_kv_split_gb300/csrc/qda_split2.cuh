@@ -15,6 +15,7 @@
 //     mlx-bun SCORE_ROW factoring, applied to V) and keeps the sum of p * B_v, so the V lanes only load them.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "qda_split.cuh"
@@ -136,16 +137,30 @@ struct Split2Geom {
   static_assert(NVL >= 1, "reduction must end with at least one score per lane");
 };
 
-// MULTI: L > 1 query positions per sequence, so the last L - 1 rows of a unit are hidden from some heads.
-template <int BITS, int D, int NH, int NG, bool EXACT, bool MULTI>
+// A score or probability rounded to the input dtype (the compat rounding points).
+__device__ __forceinline__ float round_to_input(float x, bool f16) {
+  return f16 ? __half2float(__float2half_rn(x)) : __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// MODE 0: single-pass decode. 1: single-pass with L > 1 query positions (the last L - 1 rows of a unit hidden
+// from some heads). 2: compat pass A, K only: per segment and head the (reference max, sum) of the scores rounded to
+// the input dtype. 3: compat pass B: probabilities exp(s - M) / denom from pass A's statistics, rounded to the input
+// dtype, times V, summed without rescaling (mlx-bun fused-decode-kernel.ts header: kernels A and C of the
+// two-pass form).
+template <int BITS, int D, int NH, int NG, bool EXACT, int MODE>
 __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid_constant__ QdaParams p) {
   using G = Split2Geom<BITS, D, NH>;
   constexpr int EK = G::EK, LK = G::LK, RPS = G::RPS, R = G::R, S = G::S, NV = G::NV, NVL = G::NVL;
   constexpr int EV = G::EV, KW = G::KW, VW = G::VW, W = G::W;
   constexpr int NW = QDA_NW;
-  constexpr bool EXACT_K = EXACT && BITS == 8;   // 4-bit K scores are accurate enough in the cheap form
   constexpr int LOG_NH = NH == 4 ? 2 : 1;
   constexpr int LOG_LK = LK == 32 ? 5 : 4;
+  constexpr bool MULTI = MODE == 1, STATS = MODE == 2, APPLY = MODE == 3, COMPAT = MODE >= 2;
+  // exact K codes where scores must be accurate to fp32: fp32 outputs with 8-bit codes (4-bit K scores are
+  // accurate enough in the cheap form), and the compat passes, which round every score to the input dtype and must
+  // take the same rounding decisions as a plain fp32 dot
+  constexpr bool EXACT_K = (EXACT && BITS == 8) || COMPAT;
+  constexpr float LOG2E = 1.4426950408889634f;
 
   extern __shared__ __align__(1024) unsigned char smem[];
   const int TILE = p.tile_rows, STAGES = p.stages;
@@ -230,6 +245,7 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
   float m_run = -INFINITY;  // running max of my head (equal across the lanes owning it)
   int my_hide = 0;          // last rows of the unit my head must not see (MULTI)
   float l_run = 0.f;        // sum of 2^(s - m_run) over my rows
+  float inv_den = 0.f;      // APPLY: 1 / sum of 2^(s - m_run) over the whole unit, m_run its pass-A reference
   float pb[NG];             // sum of p * B_v per group, my head
   int cur_unit = -1;
   int stage = 0, phase = 0;   // ring slot of the current chunk and the parity of its use
@@ -267,6 +283,34 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       if constexpr (MULTI) my_hide = qda_hidden_tail(hc * NH + my_h, p.nrep, p.L);
 #pragma unroll
       for (int g = 0; g < NG; ++g) pb[g] = 0.f;
+      if constexpr (APPLY) {
+        // the unit's (max, sum) from pass A's partials of every range that overlaps it, combined in a fixed order:
+        // the lanes of my head take slots in turn, then fold across those lanes
+        const long long n = walk.u_end - walk.u_start;
+        const int C = p.num_ctas;
+        const int cf = qda_cta_of(T, C, walk.u_start);
+        const int ns = qda_cta_of(T, C, walk.u_start + n - 1) - cf + 1;
+        const bool maybe_empty = T / C < 8;
+        float M = -INFINITY, den = 0.f;
+        for (int k = lane >> LOG_NH; k < ns; k += 32 >> LOG_NH) {
+          const int c = cf + k;
+          if (maybe_empty && qda_cta_row(T, C, c) == qda_cta_row(T, C, c + 1)) continue;
+          const float2 ml = p.part_ml[(size_t)(c + walk.unit) * p.heads_pad + hc * NH + my_h];
+          const float mn = fmaxf(M, ml.x);
+          den = den * ex2(M - mn) + ml.y * ex2(ml.x - mn);
+          M = mn;
+        }
+#pragma unroll
+        for (int off = NH; off < 32; off <<= 1) {
+          const float Mo = __shfl_xor_sync(0xffffffffu, M, off);
+          const float Do = __shfl_xor_sync(0xffffffffu, den, off);
+          const float mn = fmaxf(M, Mo);
+          den = (M == -INFINITY ? 0.f : den * ex2(M - mn)) + (Mo == -INFINITY ? 0.f : Do * ex2(Mo - mn));
+          M = mn;
+        }
+        m_run = M;
+        inv_den = 1.f / den;
+      }
     }
 
     const bool ok = mbar_wait_bounded(&full[stage], phase, abort_flag, p.err, 1u);
@@ -289,10 +333,12 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
         const int idx = lane + 32 * it;
         if (idx < rows_valid * NG) {
           const float2 ak = coeffs<BITS, EXACT_K>(half_bits_to_float_rt(sKS[idx], f16), half_bits_to_float_rt(sKB[idx], f16));
-          const float2 av = coeffs<BITS, EXACT>(half_bits_to_float_rt(sVS[idx], f16), half_bits_to_float_rt(sVB[idx], f16));
           reinterpret_cast<float4*>(sAB)[idx] = make_float4(ak.x, ak.x, ak.y, ak.y);
-          sAV[idx] = av.x;
-          sBV[idx] = av.y;
+          if constexpr (!STATS) {
+            const float2 av = coeffs<BITS, EXACT>(half_bits_to_float_rt(sVS[idx], f16), half_bits_to_float_rt(sVB[idx], f16));
+            sAV[idx] = av.x;
+            sBV[idx] = av.y;
+          }
         }
       }
       __syncwarp();
@@ -350,13 +396,15 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
 #pragma unroll
       for (int i = 0; i < NVL; ++i) {
         rr[i] = my_s[i] * RPS + khalf;
-        sc[i] = rr[i] < seen ? v[i] : -INFINITY;
+        float si = v[i];
+        if constexpr (COMPAT) si = round_to_input(si, f16) * LOG2E;   // natural units, rounded, then log2 units
+        sc[i] = rr[i] < seen ? si : -INFINITY;
         bm = fmaxf(bm, sc[i]);
       }
       // lazy rescaling: the reference max m_run of a head moves only when one of its scores exceeds it by more than
       // 8 (a factor 2^8 in the weights), so most blocks skip the cross-lane max and the rescale; the partial keeps
       // (m_run, sum, o) consistent whatever reference it ends with
-      const bool moved = __any_sync(0xffffffffu, bm > m_run + 8.f);
+      const bool moved = !APPLY && __any_sync(0xffffffffu, bm > m_run + 8.f);
       float alpha = 1.f;
       if (moved) {
 #pragma unroll
@@ -368,16 +416,23 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
           alpha = ex2(m_run - m_new);
         }
         m_run = m_new;
+        if constexpr (!STATS) {
 #pragma unroll
-        for (int g = 0; g < NG; ++g) pb[g] *= alpha;
+          for (int g = 0; g < NG; ++g) pb[g] *= alpha;
+        }
         l_run *= alpha;
       }
       float psum = 0.f;
 #pragma unroll
       for (int i = 0; i < NVL; ++i) {
         float2* ps = reinterpret_cast<float2*>(sPS) + 2 * (rr[i] * PS_ROW + (my_h >> 1) * NG) + (my_h & 1);
+        if constexpr (STATS) {
+          if (rr[i] < seen) psum += ex2(sc[i] - m_run);
+          continue;
+        }
         if (rr[i] < seen) {
-          const float pr = ex2(sc[i] - m_run);
+          float pr = ex2(sc[i] - m_run);
+          if constexpr (APPLY) pr = round_to_input(pr * inv_den, f16);   // normalised, rounded to the input dtype
           psum += pr;
           const float* av = sAV + rr[i] * NG;
           const float* bv = sBV + rr[i] * NG;
@@ -395,7 +450,8 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       l_run += psum;
       __syncwarp();
 
-      // ---- phase 4: V accumulation
+      // ---- phase 4: V accumulation (none in pass A)
+      if constexpr (STATS) continue;
       if (moved) {
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
@@ -433,34 +489,42 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
 #pragma unroll
       for (int off = NH; off < 32; off <<= 1) {
         l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
+        if constexpr (!STATS) {
 #pragma unroll
-        for (int g = 0; g < NG; ++g) pb[g] += __shfl_xor_sync(0xffffffffu, pb[g], off);
+          for (int g = 0; g < NG; ++g) pb[g] += __shfl_xor_sync(0xffffffffu, pb[g], off);
+        }
       }
-      if (lane < NH) {   // lane < NH owns head my_h; all heads are covered once
+      if constexpr (!STATS) {
+        if (lane < NH) {   // lane < NH owns head my_h; all heads are covered once
 #pragma unroll
-        for (int g = 0; g < NG; ++g) sPB[my_h * NG + g] = pb[g];
-      }
-      __syncwarp();
+          for (int g = 0; g < NG; ++g) sPB[my_h * NG + g] = pb[g];
+        }
+        __syncwarp();
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        const float b = sPB[h * NG + gv];
+        for (int h = 0; h < NH; ++h) {
+          const float b = sPB[h * NG + gv];
 #pragma unroll
-        for (int k = 0; k < EV / 2; ++k) o[h][k] = __fadd2_rn(o[h][k], make_float2(b, b));
+          for (int k = 0; k < EV / 2; ++k) o[h][k] = __fadd2_rn(o[h][k], make_float2(b, b));
+        }
       }
       named_barrier_sync(1, NW * 32);   // every warp is done with its scratch before it becomes the combine area
+      if constexpr (!STATS) {
 #pragma unroll
-      for (int h = 0; h < NH; ++h)
+        for (int h = 0; h < NH; ++h)
 #pragma unroll
-        for (int k = 0; k < EV / 2; ++k)
-          reinterpret_cast<float2*>(comb_o + (warp * NH + h) * D + lane * EV)[k] = o[h][k];
+          for (int k = 0; k < EV / 2; ++k)
+            reinterpret_cast<float2*>(comb_o + (warp * NH + h) * D + lane * EV)[k] = o[h][k];
+      }
       if (lane < NH) {
         comb_m[warp * NH + my_h] = m_run;
         comb_l[warp * NH + my_h] = l_run;
       }
       named_barrier_sync(1, NW * 32);
       const long long slot = (long long)cta + walk.unit;
-      for (int idx = threadIdx.x; idx < NH * D; idx += NW * 32) {
-        const int h = idx / D, d = idx - h * D;
+      // pass A writes only (max, sum) per head; pass B only o (its weights are already normalised, and other CTAs
+      // of pass B may still be reading pass A's statistics)
+      for (int idx = threadIdx.x; idx < (STATS ? NH : NH * D); idx += NW * 32) {
+        const int h = STATS ? idx : idx / D, d = STATS ? 0 : idx - h * D;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < NW; ++w) M = fmaxf(M, comb_m[w * NH + h]);
@@ -468,13 +532,13 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
           const float mw = comb_m[w * NH + h];
-          const float wt = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-          O = fmaf(comb_o[(w * NH + h) * D + d], wt, O);
+          const float wt = APPLY ? 1.f : (mw == -INFINITY) ? 0.f : ex2(mw - M);
+          if constexpr (!STATS) O = fmaf(comb_o[(w * NH + h) * D + d], wt, O);
           Ls = fmaf(comb_l[w * NH + h], wt, Ls);
         }
         const size_t hp = (size_t)slot * p.heads_pad + (size_t)hc * NH + h;
-        p.part_o[hp * D + d] = O;
-        if (d == 0) p.part_ml[hp] = make_float2(M, Ls);
+        if constexpr (!STATS) p.part_o[hp * D + d] = O;
+        if (!APPLY && d == 0) p.part_ml[hp] = make_float2(M, Ls);
       }
       named_barrier_sync(1, NW * 32);
     }
@@ -485,10 +549,10 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
   }
 }
 
-template <int BITS, bool EXACT, bool MULTI, typename Fn>
+template <int BITS, bool EXACT, int MODE, typename Fn>
 cudaError_t with_split2_kernel_m(int D, int nh, int ng, Fn&& f) {
 #define QDA_V2(D_, NH_, NG_) \
-  if (D == D_ && nh == NH_ && ng == NG_) return f(qda_split2_kernel<BITS, D_, NH_, NG_, EXACT, MULTI>);
+  if (D == D_ && nh == NH_ && ng == NG_) return f(qda_split2_kernel<BITS, D_, NH_, NG_, EXACT, MODE>);
   QDA_V2(256, 2, 2) QDA_V2(256, 2, 4) QDA_V2(256, 2, 8)
   QDA_V2(256, 4, 2) QDA_V2(256, 4, 4) QDA_V2(256, 4, 8)
   QDA_V2(512, 2, 4) QDA_V2(512, 2, 8) QDA_V2(512, 2, 16)
@@ -497,14 +561,19 @@ cudaError_t with_split2_kernel_m(int D, int nh, int ng, Fn&& f) {
 }
 
 template <int BITS, bool EXACT, typename Fn>
-cudaError_t with_split2_kernel(int D, int nh, int ng, bool multi, Fn&& f) {
-  return multi ? with_split2_kernel_m<BITS, EXACT, true>(D, nh, ng, f)
-               : with_split2_kernel_m<BITS, EXACT, false>(D, nh, ng, f);
+cudaError_t with_split2_kernel(int D, int nh, int ng, int mode, Fn&& f) {
+  switch (mode) {
+    case 0: return with_split2_kernel_m<BITS, EXACT, 0>(D, nh, ng, f);
+    case 1: return with_split2_kernel_m<BITS, EXACT, 1>(D, nh, ng, f);
+    case 2: return with_split2_kernel_m<BITS, false, 2>(D, nh, ng, f);   // pass A reads no V: no exact variant
+    case 3: return with_split2_kernel_m<BITS, EXACT, 3>(D, nh, ng, f);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int BITS, bool EXACT>
 cudaError_t launch_split2(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem, cudaStream_t s) {
-  return with_split2_kernel<BITS, EXACT>(D, nh, ng, p.L > 1, [&](auto kern) -> cudaError_t {
+  return with_split2_kernel<BITS, EXACT>(D, nh, ng, p.mode, [&](auto kern) -> cudaError_t {
     cudaError_t e = ensure_smem_limit(kern, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, QDA_THREADS, smem, s>>>(p);
@@ -515,7 +584,7 @@ cudaError_t launch_split2(const QdaParams& p, int D, int nh, int ng, dim3 grid, 
 template <int BITS, bool EXACT>
 cudaError_t occupancy_split2(int D, int nh, int ng, size_t smem, int* n) {
   // both instances of a shape have the same resources; the single-query one stands for both
-  return with_split2_kernel<BITS, EXACT>(D, nh, ng, false, [&](auto kern) -> cudaError_t {
+  return with_split2_kernel<BITS, EXACT>(D, nh, ng, 0, [&](auto kern) -> cudaError_t {
     cudaError_t e = ensure_smem_limit(kern, smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, QDA_THREADS, smem);

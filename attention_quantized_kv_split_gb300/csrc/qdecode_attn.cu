@@ -255,9 +255,11 @@ int plan_impl(int B, int L, int H, int Hkv, const int32_t* N, int D, int GS, int
 enum class Scratch { kWorkspace, kStatic };
 
 // Every decode entry point: checks, plan, scratch, parameters, the split and merge launches.
+// compat: the two-pass form with the pages' rounding points (lean kernel shapes, one query position).
 int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
              const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out, int B, int L, int H,
-             int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream, Scratch where) {
+             int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream, Scratch where,
+             bool compat = false) {
   if (!q || !k_packed || !k_scales || !k_biases || !v_packed || !v_scales || !v_biases || !out)
     return QDA_ERR_INVALID;
   int in_dt, out_dt;
@@ -269,11 +271,12 @@ int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, cons
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return QDA_ERR_ALIGN;
 
+  const int nrep = H / Hkv;
+  const Variant v = pick_variant(nrep * L, D, GS, bits);
+  if (compat && (v.kind != 2 || L != 1)) return QDA_ERR_UNSUPPORTED;
   int dev;
   DeviceState* d = device_state(&dev);
   if (d == nullptr) return QDA_ERR_CUDA;
-  const int nrep = H / Hkv;
-  const Variant v = pick_variant(nrep * L, D, GS, bits);
   const bool exact = out_dt == QDA_FP32;
   int occ = 1;
   st = occupancy_for(*d, bits, D, exact, v, &occ);
@@ -342,12 +345,26 @@ int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, cons
   p.tile_shift = 0;
   while ((1 << p.tile_shift) < v.tile) ++p.tile_shift;
   p.f16 = in_dt == QDA_FP16 ? 1 : 0;
-  p.qscale = 1.4426950408889634f / sqrtf((float)D);
+  // scores in log2 units, except in the compat form, which rounds them in natural units first
+  p.qscale = (compat ? 1.0f : 1.4426950408889634f) / sqrtf((float)D);
   p.seq_off[0] = 0;
   for (int b = 0; b < B; ++b) p.seq_off[b + 1] = p.seq_off[b] + N[b];
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = split_launch(bits, exact, p, v, dim3((unsigned)plan.num_ctas * (unsigned)v.hc), s);
+  const dim3 grid((unsigned)plan.num_ctas * (unsigned)v.hc);
+  cudaError_t e;
+  if (compat) {
+    p.mode = 2;   // pass A: K only, per-range statistics of the rounded scores
+    p.k_only = 1;
+    e = split_launch(bits, exact, p, v, grid, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    p.mode = 3;   // pass B: normalised, rounded probabilities times V
+    p.k_only = 0;
+    p.compat = 1;
+  } else {
+    p.mode = L > 1 ? 1 : 0;
+  }
+  e = split_launch(bits, exact, p, v, grid, s);
   if (e != cudaSuccess) return cuda_fail(e);
   const bool use_event = t_split_event != nullptr && where == Scratch::kWorkspace;
   if (use_event) {
@@ -417,6 +434,13 @@ int qdecode_attn_multi(const void* q, const uint32_t* k_packed, const void* k_sc
                        int H, int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream) {
   return run_call(q, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, out, B, L, H, Hkv, N, D, GS, bits,
                   dtype, stream, Scratch::kWorkspace);
+}
+
+int qdecode_attn_compat(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
+                        const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out, int B,
+                        int H, int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream) {
+  return run_call(q, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, out, B, 1, H, Hkv, N, D, GS, bits,
+                  dtype, stream, Scratch::kWorkspace, true);
 }
 
 // The allocation-free entry point: partial results in the fixed device array above, never in an allocation.

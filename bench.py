@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2)
-    ap.add_argument("--no-extra", action="store_true", help="skip the per-workload figures (workloads 3-5 and 4-position multi-query decode)")
+    ap.add_argument("--no-extra", action="store_true", help="skip the per-workload figures (workloads 3-5, 4-position multi-query decode, two-pass compat form)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -363,6 +363,18 @@ def run_ours(args):
                               "frac_of_peak": round(bx / (mx * 1e-3) / 1e9 / peak, 4), "kv_bytes": bx}
             del cx, qx, ox
             torch.cuda.empty_cache()
+        # the two-pass compat form on this workload's cache (K read in both passes)
+        if w.D in (256, 512):
+            oc = torch.empty_like(out)
+            ccall = lambda: qda.qdecode_attn_compat(q, cache.kp, cache.ks, cache.kb, cache.vp, cache.vs, cache.vb, oc,
+                                                    N, w.Hkv, w.GS, w.bits, stream)
+            for _ in range(5):
+                ccall()
+            mc = statistics.median(time_calls(ccall, 50, flush, stream))
+            extra[f"{w.name}_two_pass_compat"] = {
+                "us_per_call": round(mc * 1e3, 2), "kv_GBps": round(nbytes / (mc * 1e-3) / 1e9, 1),
+                "frac_of_peak": round(nbytes / (mc * 1e-3) / 1e9 / peak, 4), "kv_bytes": nbytes,
+                "note": "K is read in both passes; kv_GBps counts each KV byte once"}
         # small-L multi-query decode on this workload's cache: 4 query positions (the last 4 tokens) per sequence
         Lq = 4
         qm = synth.query_multi(w, Lq).to(device)

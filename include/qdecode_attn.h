@@ -118,6 +118,23 @@ int qdecode_attn_multi(const void* q, const uint32_t* k_packed, const void* k_sc
                        int B, int L, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int dtype,
                        void* stream);
 
+/*
+ * qdecode_attn_compat: the same attention in the pages' two-pass form with their compat rounding points
+ * (mlx-bun fused-decode-kernel.ts, header comment: kernel A takes per-block (max, sum-exp) over scores rounded to T,
+ * kernel C sums T(exp(s - M) / denom) * dequant(V) with the full-row (M, denom), the merge sums the blocks and
+ * casts to T), for comparison with MLX-style unfused paths. T is the input dtype. Per query head:
+ *
+ *     s_n = T(q . k_hat_n / sqrt(D))   (fp32 dot, rounded to T)
+ *     p_n = T(exp(s_n - M) / denom)    (M = max_n s_n, denom = sum_n exp(s_n - M), fp32)
+ *     out = sum_n p_n * v_hat_n        (fp32, not renormalised, rounded to the output dtype)
+ *
+ * K is read twice (once per pass), V once. Arguments, layouts, workspace, stream and errors as for qdecode_attn;
+ * supported for D in {256, 512} (QDA_ERR_UNSUPPORTED otherwise).
+ */
+int qdecode_attn_compat(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
+                        const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out,
+                        int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream);
+
 /* The launch plan qdecode_attn would use (host only). Determined by the shape and the GPU alone. */
 typedef struct {
   int num_ctas;           /* CTAs along the flattened row space (each takes one contiguous row range) */
