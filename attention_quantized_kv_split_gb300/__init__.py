@@ -70,7 +70,7 @@ def qdecode_attn_compat(q: torch.Tensor, k_packed: torch.Tensor, k_scales: torch
                         v_packed: torch.Tensor, v_scales: torch.Tensor, v_biases: torch.Tensor, out: torch.Tensor,
                         N: Sequence[int], Hkv: int, GS: int, bits: int, stream=None) -> torch.Tensor:
     """qdecode_attn in the two-pass form with compat rounding: scores and normalised probabilities rounded to the
-    input dtype, the probability-weighted V rows summed without renormalising (D in {256, 512})."""
+    input dtype, the probability-weighted V rows summed without renormalising."""
     B, H, D = q.shape
     st = lib().qdecode_attn_compat(_ptr(q), _ptr(k_packed), _ptr(k_scales), _ptr(k_biases), _ptr(v_packed),
                                    _ptr(v_scales), _ptr(v_biases), _ptr(out), B, H, Hkv, _lib.int32_array(N), D,

@@ -14,6 +14,7 @@
 // one partial (max, sum, o[D]) per query head in the workspace slot (cta + unit), merged by the merge kernel.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <mutex>
@@ -29,6 +30,39 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// A score or probability rounded to the input dtype (the compat rounding points of the two-pass form).
+__device__ __forceinline__ float round_to_input(float x, bool f16) {
+  return f16 ? __half2float(__float2half_rn(x)) : __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// The (max, sum) of one head's scores over a whole unit, from pass A's per-range partials (compat pass B): the 32
+// lanes take the unit's slots in turn and fold across the warp in a fixed order. Every lane gets the result.
+__device__ __forceinline__ void unit_stats(const QdaParams& p, long long T, long long u_start, long long u_end,
+                                           int unit, int head, float& M, float& den) {
+  const int C = p.num_ctas;
+  const int cf = qda_cta_of(T, C, u_start);
+  const int ns = qda_cta_of(T, C, u_end - 1) - cf + 1;
+  const bool maybe_empty = T / C < 8;   // only ranges shorter than 8 rows can be empty (and wrote no slot)
+  M = -INFINITY;
+  den = 0.f;
+  for (int k = threadIdx.x & 31; k < ns; k += 32) {
+    const int c = cf + k;
+    if (maybe_empty && qda_cta_row(T, C, c) == qda_cta_row(T, C, c + 1)) continue;
+    const float2 ml = p.part_ml[(size_t)(c + unit) * p.heads_pad + head];
+    const float mn = fmaxf(M, ml.x);
+    den = (M == -INFINITY ? 0.f : den * exp2f(M - mn)) + ml.y * exp2f(ml.x - mn);
+    M = mn;
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const float Mo = __shfl_xor_sync(0xffffffffu, M, off);
+    const float Do = __shfl_xor_sync(0xffffffffu, den, off);
+    const float mn = fmaxf(M, Mo);
+    den = (M == -INFINITY ? 0.f : den * exp2f(M - mn)) + (Mo == -INFINITY ? 0.f : Do * exp2f(Mo - mn));
+    M = mn;
+  }
 }
 
 // Iterates the chunks of one CTA's row range. A chunk is the intersection of one pipeline tile (tile_rows rows,
@@ -152,9 +186,13 @@ __device__ __forceinline__ void produce_range(const QdaParams& p, ChunkWalker wa
 }
 
 // BITS: 4 or 8. WPL: packed words per lane per row. LPR: lanes per row (RPS = 32/LPR rows per warp step).
-// NH: query heads per CTA. D = LPR * WPL * 32 / BITS.
-template <int BITS, int WPL, int LPR, int NH>
+// NH: query heads per CTA. D = LPR * WPL * 32 / BITS. MODE: 0 single-pass (any L), 2 compat pass A (K only,
+// per-range (max, sum) of the scores rounded to the input dtype), 3 compat pass B (rounded exp(s - M) / denom times
+// V, summed without rescaling).
+template <int BITS, int WPL, int LPR, int NH, int MODE = 0>
 __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_constant__ QdaParams p) {
+  constexpr bool STATS = MODE == 2, APPLY = MODE == 3, COMPAT = MODE >= 2;
+  constexpr float LOG2E = 1.4426950408889634f;
   constexpr int PER = 32 / BITS;          // codes per word
   constexpr int E = WPL * PER;            // elements per lane per row
   constexpr int RPS = 32 / LPR;           // rows per warp step
@@ -207,6 +245,7 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
   const int lir = lane % LPR;     // lane's slice of the row: elements [lir*E, lir*E + E)
   float qv[NH][E], qsum[NH], o[NH][E], m[NH], l[NH];
   int hide[NH];   // last rows of the unit each head must not see (multi-query decode)
+  float inv[NH];  // APPLY: 1 / the unit's sum of 2^(s - m) per head
   int cur_unit = -1;
   int s = 0, phase = 0;   // ring slot of the current chunk and the parity of its use
   while (walk.next(p, c0, c1, t0)) {
@@ -234,6 +273,11 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
         l[h] = 0.f;
 #pragma unroll
         for (int e = 0; e < E; ++e) o[h][e] = 0.f;
+        if constexpr (APPLY) {   // pass B: the unit's statistics from pass A fix every weight in advance
+          float den;
+          unit_stats(p, T, walk.u_start, walk.u_end, walk.unit, hc * NH + h, m[h], den);
+          inv[h] = 1.f / den;
+        }
       }
     }
     const bool ok = mbar_wait_bounded(&full[s], phase, abort_flag, p.err, 1u);
@@ -279,7 +323,14 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
           const bool seen = valid && row < walk.u_end - hide[h];
-          const float sh = seen ? sc[h] : -INFINITY;
+          float sv = sc[h];
+          if constexpr (COMPAT) sv = round_to_input(sv, f16) * LOG2E;   // natural units, rounded, then log2 units
+          const float sh = seen ? sv : -INFINITY;
+          if constexpr (APPLY) {
+            alpha[h] = 1.f;
+            pr[h] = seen ? round_to_input(ex2(sh - m[h]) * inv[h], f16) : 0.f;
+            continue;
+          }
           float mx = sh;
 #pragma unroll
           for (int off = LPR; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -294,21 +345,23 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
           m[h] = mn;
           l[h] = fmaf(l[h], alpha[h], pr[h]);
         }
-        // V: o = alpha * o + p * (s * c + b)
+        // V: o = alpha * o + p * (s * c + b) (none in compat pass A)
+        if constexpr (!STATS) {
 #pragma unroll
-        for (int w = 0; w < WPL; ++w) {
-          const uint32_t word = sV[lr * W + lir * WPL + w];
+          for (int w = 0; w < WPL; ++w) {
+            const uint32_t word = sV[lr * W + lir * WPL + w];
 #pragma unroll
-          for (int k = 0; k < PER; ++k)
-            cf[w * PER + k] = __uint_as_float(0x4B000000u | ((word >> (BITS * k)) & MASK)) - 8388608.0f;
-        }
-        const float vsc = half_bits_to_float_rt(sVS[lr * NG + g], f16);
-        const float vbi = half_bits_to_float_rt(sVB[lr * NG + g], f16);
+            for (int k = 0; k < PER; ++k)
+              cf[w * PER + k] = __uint_as_float(0x4B000000u | ((word >> (BITS * k)) & MASK)) - 8388608.0f;
+          }
+          const float vsc = half_bits_to_float_rt(sVS[lr * NG + g], f16);
+          const float vbi = half_bits_to_float_rt(sVB[lr * NG + g], f16);
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const float ps = pr[h] * vsc, pb = pr[h] * vbi;
+          for (int h = 0; h < NH; ++h) {
+            const float ps = pr[h] * vsc, pb = pr[h] * vbi;
 #pragma unroll
-          for (int e = 0; e < E; ++e) o[h][e] = fmaf(o[h][e], alpha[h], fmaf(ps, cf[e], pb));
+            for (int e = 0; e < E; ++e) o[h][e] = fmaf(o[h][e], alpha[h], fmaf(ps, cf[e], pb));
+          }
         }
       }
     }
@@ -323,12 +376,14 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
             l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+            if constexpr (!STATS) {
 #pragma unroll
-            for (int e = 0; e < E; ++e) o[h][e] += __shfl_xor_sync(0xffffffffu, o[h][e], off);
+              for (int e = 0; e < E; ++e) o[h][e] += __shfl_xor_sync(0xffffffffu, o[h][e], off);
+            }
           }
         }
       }
-      if (rir == 0) {
+      if (!STATS && rir == 0) {
 #pragma unroll
         for (int h = 0; h < NH; ++h)
 #pragma unroll
@@ -343,8 +398,10 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
       }
       named_barrier_sync(1, NW * 32);
       const long long slot = (long long)cta + walk.unit;
-      for (int idx = threadIdx.x; idx < NH * D; idx += NW * 32) {
-        const int h = idx / D, d = idx - h * D;
+      // compat pass A writes only (max, sum) per head; pass B only o (other CTAs of pass B may still be reading
+      // pass A's statistics)
+      for (int idx = threadIdx.x; idx < (STATS ? NH : NH * D); idx += NW * 32) {
+        const int h = STATS ? idx : idx / D, d = STATS ? 0 : idx - h * D;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < NW; ++w) M = fmaxf(M, comb_m[w * NH + h]);
@@ -352,13 +409,13 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
           const float mw = comb_m[w * NH + h];
-          const float wt = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-          O = fmaf(comb_o[(w * NH + h) * D + d], wt, O);
+          const float wt = APPLY ? 1.f : (mw == -INFINITY) ? 0.f : ex2(mw - M);
+          if constexpr (!STATS) O = fmaf(comb_o[(w * NH + h) * D + d], wt, O);
           Ls = fmaf(comb_l[w * NH + h], wt, Ls);
         }
         const size_t hp = (size_t)slot * p.heads_pad + (size_t)hc * NH + h;
-        p.part_o[hp * D + d] = O;
-        if (d == 0) p.part_ml[hp] = make_float2(M, Ls);
+        if constexpr (!STATS) p.part_o[hp * D + d] = O;
+        if (!APPLY && d == 0) p.part_ml[hp] = make_float2(M, Ls);
       }
       named_barrier_sync(1, NW * 32);
     }
@@ -370,15 +427,15 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
 }
 
 // Calls f(kernel) with the instantiation for (wpl, lpr, nh); returns cudaErrorInvalidValue for an unbuilt one.
-template <int BITS, typename Fn>
-cudaError_t with_split_kernel(int wpl, int lpr, int nh, Fn&& f) {
+template <int BITS, int MODE, typename Fn>
+cudaError_t with_split_kernel_m(int wpl, int lpr, int nh, Fn&& f) {
 #define QDA_NH_CASES(WPL_, LPR_)                                                        \
   switch (nh) {                                                                         \
-    case 1: return f(qda_split_kernel<BITS, WPL_, LPR_, 1>);                       \
-    case 2: return f(qda_split_kernel<BITS, WPL_, LPR_, 2>);                       \
-    case 4: return f(qda_split_kernel<BITS, WPL_, LPR_, 4>);                       \
+    case 1: return f(qda_split_kernel<BITS, WPL_, LPR_, 1, MODE>);                 \
+    case 2: return f(qda_split_kernel<BITS, WPL_, LPR_, 2, MODE>);                 \
+    case 4: return f(qda_split_kernel<BITS, WPL_, LPR_, 4, MODE>);                 \
     case 8:                                                                             \
-      if constexpr (WPL_ * (32 / BITS) * 8 <= 64) return f(qda_split_kernel<BITS, WPL_, LPR_, 8>); \
+      if constexpr (WPL_ * (32 / BITS) * 8 <= 64) return f(qda_split_kernel<BITS, WPL_, LPR_, 8, MODE>); \
       else return cudaErrorInvalidValue;                                                \
     default: return cudaErrorInvalidValue;                                              \
   }
@@ -395,6 +452,18 @@ cudaError_t with_split_kernel(int wpl, int lpr, int nh, Fn&& f) {
   }
 #undef QDA_NH_CASES
   return cudaErrorInvalidValue;
+}
+
+// The general kernel serves D in {64, 128} (and any shape the lean kernel does not take); mode 1 (multi-query)
+// runs as mode 0, which masks at run time.
+template <int BITS, typename Fn>
+cudaError_t with_split_kernel(int wpl, int lpr, int nh, int mode, Fn&& f) {
+  switch (mode) {
+    case 0: case 1: return with_split_kernel_m<BITS, 0>(wpl, lpr, nh, f);
+    case 2: return with_split_kernel_m<BITS, 2>(wpl, lpr, nh, f);
+    case 3: return with_split_kernel_m<BITS, 3>(wpl, lpr, nh, f);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // Raises a kernel's dynamic shared-memory limit to the opt-in maximum, once per (kernel, device).
@@ -417,7 +486,7 @@ cudaError_t ensure_smem_limit(K kern, size_t smem) {
 
 template <int BITS>
 cudaError_t launch_split(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s) {
-  return with_split_kernel<BITS>(wpl, lpr, nh, [&](auto kern) -> cudaError_t {
+  return with_split_kernel<BITS>(wpl, lpr, nh, p.mode, [&](auto kern) -> cudaError_t {
     cudaError_t e = ensure_smem_limit(kern, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, QDA_THREADS, smem, s>>>(p);
@@ -427,7 +496,7 @@ cudaError_t launch_split(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid
 
 template <int BITS>
 cudaError_t occupancy_split(int wpl, int lpr, int nh, size_t smem, int* n) {
-  return with_split_kernel<BITS>(wpl, lpr, nh, [&](auto kern) -> cudaError_t {
+  return with_split_kernel<BITS>(wpl, lpr, nh, 0, [&](auto kern) -> cudaError_t {
     cudaError_t e = ensure_smem_limit(kern, smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, QDA_THREADS, smem);

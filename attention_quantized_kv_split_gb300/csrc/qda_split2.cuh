@@ -137,11 +137,6 @@ struct Split2Geom {
   static_assert(NVL >= 1, "reduction must end with at least one score per lane");
 };
 
-// A score or probability rounded to the input dtype (the compat rounding points).
-__device__ __forceinline__ float round_to_input(float x, bool f16) {
-  return f16 ? __half2float(__float2half_rn(x)) : __bfloat162float(__float2bfloat16_rn(x));
-}
-
 // MODE 0: single-pass decode. 1: single-pass with L > 1 query positions (the last L - 1 rows of a unit hidden
 // from some heads). 2: compat pass A, K only: per segment and head the (reference max, sum) of the scores rounded to
 // the input dtype. 3: compat pass B: probabilities exp(s - M) / denom from pass A's statistics, rounded to the input

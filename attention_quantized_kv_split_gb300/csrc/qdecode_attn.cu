@@ -255,7 +255,7 @@ int plan_impl(int B, int L, int H, int Hkv, const int32_t* N, int D, int GS, int
 enum class Scratch { kWorkspace, kStatic };
 
 // Every decode entry point: checks, plan, scratch, parameters, the split and merge launches.
-// compat: the two-pass form with the pages' rounding points (lean kernel shapes, one query position).
+// compat: the two-pass form with the pages' rounding points (one query position).
 int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
              const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out, int B, int L, int H,
              int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream, Scratch where,
@@ -273,7 +273,7 @@ int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, cons
 
   const int nrep = H / Hkv;
   const Variant v = pick_variant(nrep * L, D, GS, bits);
-  if (compat && (v.kind != 2 || L != 1)) return QDA_ERR_UNSUPPORTED;
+  if (compat && L != 1) return QDA_ERR_UNSUPPORTED;
   int dev;
   DeviceState* d = device_state(&dev);
   if (d == nullptr) return QDA_ERR_CUDA;

@@ -128,8 +128,8 @@ int qdecode_attn_multi(const void* q, const uint32_t* k_packed, const void* k_sc
  *     p_n = T(exp(s_n - M) / denom)    (M = max_n s_n, denom = sum_n exp(s_n - M), fp32)
  *     out = sum_n p_n * v_hat_n        (fp32, not renormalised, rounded to the output dtype)
  *
- * K is read twice (once per pass), V once. Arguments, layouts, workspace, stream and errors as for qdecode_attn;
- * supported for D in {256, 512} (QDA_ERR_UNSUPPORTED otherwise).
+ * K is read twice (once per pass), V once. Arguments, layouts, supported shapes, workspace, stream and errors as for
+ * qdecode_attn.
  */
 int qdecode_attn_compat(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
                         const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out,

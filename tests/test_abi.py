@@ -232,9 +232,8 @@ def test_multi_plan_serves_every_position(L, shape, Lq):
 def test_compat_argument_errors(L):
     p = [FAKE + 256 * i for i in range(8)]
     n = _lib.int32_array([64])
-    # the two-pass compat form runs on the lean kernel only (D in {256, 512})
-    assert L.qdecode_attn_compat(*p, 1, 8, 2, n, 128, 32, 4, 1, None) == _lib.QDA_ERR_UNSUPPORTED
-    assert L.qdecode_attn_compat(*p, 1, 8, 2, n, 64, 32, 8, 1, None) == _lib.QDA_ERR_UNSUPPORTED
+    assert L.qdecode_attn_compat(*p, 1, 8, 2, n, 96, 32, 4, 1, None) == _lib.QDA_ERR_UNSUPPORTED
+    assert L.qdecode_attn_compat(*p, 1, 8, 2, n, 64, 32, 3, 1, None) == _lib.QDA_ERR_UNSUPPORTED
     assert L.qdecode_attn_compat(*p, 1, 8, 3, n, 256, 32, 4, 1, None) == _lib.QDA_ERR_INVALID
     assert L.qdecode_attn_compat(*p, 1, 8, 2, n, 256, 48, 4, 1, None) == _lib.QDA_ERR_UNSUPPORTED
     q = list(p)

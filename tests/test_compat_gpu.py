@@ -12,7 +12,7 @@ import torch
 
 import oracle as O
 import attention_quantized_kv_split_gb300 as qda
-from attention_quantized_kv_split_gb300 import _lib, build, synth
+from attention_quantized_kv_split_gb300 import build, synth
 
 from harness import TORCH_DT, gpu_quantized_workload, small_case, unit_oracle_cache, upload_cache
 
@@ -59,7 +59,7 @@ def check(w, out_dtype=None, splits=0):
     return out, (q, dev, N)
 
 
-SHAPES = [(D, bits, GS) for D in (256, 512) for bits in (4, 8) for GS in (32, 64, 128)]
+SHAPES = [(D, bits, GS) for D in (64, 128, 256, 512) for bits in (4, 8) for GS in (32, 64, 128) if D % GS == 0]
 
 
 @pytest.mark.parametrize("N", [1, 33, 257, 3000])
@@ -142,13 +142,12 @@ def test_compat_differs_from_exact_softmax_where_rounding_matters():
     assert abs(out_e[0, 0, 5].item() - ref_e[5]) <= 1e-4 * np.abs(ref_e).max()
 
 
-def test_compat_rejects_shapes_without_the_lean_kernel():
-    w = synth.small(B=1, H=4, Hkv=2, D=128, N=(64,), bits=4, GS=32)
-    q, cache, N = small_case(w)
-    dev = upload_cache(*cache, w.dtype_in)
-    with pytest.raises(_lib.QdaError) as e:
-        run_compat(q, dev, N, w)
-    assert e.value.status == _lib.QDA_ERR_UNSUPPORTED
+@pytest.mark.parametrize("D", [64, 128])
+def test_compat_general_kernel_gqa_and_splits(D):
+    # D = 64 and 128 run on the general split kernel
+    check(synth.small(B=2, H=24, Hkv=3, D=D, N=(900, 50), bits=8, GS=32, seed=D))
+    check(synth.small(B=2, H=8, Hkv=2, D=D, N=(300, 77), bits=4, GS=32, dtype_in="fp16", seed=D + 1), "fp32",
+          splits=37)
 
 
 def test_compat_8k_workload_sampled():
