@@ -17,6 +17,7 @@ from .qda_oracle import (  # noqa: F401
     dequantize,
     from_bits16,
     pack,
+    qgemv,
     quantize,
     quantize_cache,
     round_to,

@@ -23,6 +23,7 @@ What it computes, step by step, in the order of the method's description:
    attending the rows up to its own (``visible_rows``); L = 1 is step 4.
 7. ``attention_head_compat`` / ``attention_two_pass_blocked`` / ``attention_packed_compat``: the two-pass variant
    with the pages' compat rounding points (scores and normalised probabilities rounded to the input dtype T).
+8. ``qgemv``: the same affine codec under a plain matrix-vector product (a comparison workload).
 
 Readings taken where the pages are silent (each pinned by a test in ``tests/test_oracle.py``):
 
@@ -328,6 +329,18 @@ def attention_packed_compat(q, kp, ks, kb, vp, vs, vb, N, H: int, Hkv: int, D: i
         Kd, Vd = cache[key]
         res[(b, h)] = attention_head_compat(q[b, h], Kd, Vd, dtype)
     return res
+
+
+def qgemv(x, wp, ws, wb, K: int, GS: int, bits: int) -> np.ndarray:
+    """Matrix-vector product with an affine-quantized weight matrix, fp64 (maya-mac ``mlx_kernels.py``,
+    ``_linear_kernel``: each weight is ``code * scale + bias`` with one scale and bias per group of GS consecutive
+    elements of a row, codes packed LSB-first; ``y[t, n] = sum_k x[t, k] * w[n, k]``, here without the kernel's
+    optional LayerNorm, activation and residual epilogues).
+
+    x ``[T, K]`` (values); wp ``[N, K*bits/32]`` uint32; ws, wb ``[N, K/GS]`` (values). Returns y ``[T, N]``.
+    """
+    W = dequantize(unpack(wp, bits, K), ws, wb, GS)
+    return np.asarray(x, np.float64) @ W.T
 
 
 def quantize_cache(K, V, GS: int, bits: int, dtype: str):

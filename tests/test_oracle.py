@@ -433,3 +433,45 @@ def test_compat_packed_interface():
             K = O.dequantize(O.unpack(kp[r0:r1], bits, D), ks[r0:r1], kb[r0:r1], GS)
             V = O.dequantize(O.unpack(vp[r0:r1], bits, D), vs[r0:r1], vb[r0:r1], GS)
             np.testing.assert_array_equal(got[(b, h)], O.attention_head_compat(q[b, h], K, V, "bf16"))
+
+
+# --------------------------------------------------------------- affine-quantized weight GEMV (comparison workload)
+
+
+def test_qgemv_closed_form_integer_codes():
+    # a group [0, 1, ..., GS-1] repeated: scale 1, bias 0, codes = the integers; x = 1 gives the row sums
+    K, GS, N = 256, 64, 3
+    row = np.tile(np.arange(GS, dtype=np.float32) * (255 / (GS - 1)), K // GS)
+    row = np.round(row)                                 # integers 0..255 with min 0 and max 255
+    w = np.stack([row] * N).astype(np.float32)
+    c, s, b = O.quantize(w, GS, 8, "bf16")
+    assert np.all(s == 1.0) and np.all(b == 0.0)
+    y = O.qgemv(np.ones((2, K)), O.pack(c, 8), s, b, K, GS, 8)
+    np.testing.assert_array_equal(y, np.full((2, N), row.sum()))
+
+
+def test_qgemv_bias_only_rows():
+    # all codes 0: y[t, n] = sum_g b[n, g] * sum_{k in g} x[t, k]
+    rng = np.random.default_rng(41)
+    T, N, K, GS = 3, 5, 128, 32
+    wp = np.zeros((N, K * 4 // 32), np.uint32)
+    ws = rng.uniform(0.1, 1, (N, K // GS))
+    wb = rng.standard_normal((N, K // GS))
+    x = rng.standard_normal((T, K))
+    y = O.qgemv(x, wp, ws, wb, K, GS, 4)
+    ref = np.einsum("ng,tg->tn", wb, x.reshape(T, K // GS, GS).sum(-1))
+    np.testing.assert_allclose(y, ref, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_qgemv_brute_force_loops(bits):
+    rng = np.random.default_rng(42 + bits)
+    T, N, K, GS = 2, 3, 64, 32
+    w = rng.standard_normal((N, K)).astype(np.float32)
+    c, s, b = O.quantize(w, GS, bits, "fp16")
+    x = rng.standard_normal((T, K))
+    y = O.qgemv(x, O.pack(c, bits), s, b, K, GS, bits)
+    for t in range(T):
+        for n in range(N):
+            ref = sum(float(x[t, k]) * (float(c[n, k]) * float(s[n, k // GS]) + float(b[n, k // GS])) for k in range(K))
+            assert abs(y[t, n] - ref) <= 1e-12 * max(1.0, abs(ref))
