@@ -161,6 +161,18 @@ def qdecode_quantize(x: torch.Tensor, GS: int, bits: int, dtype: torch.dtype, pa
     _lib.check(st, "qdecode_quantize")
 
 
+def qdecode_qgemv(x: torch.Tensor, w_packed: torch.Tensor, w_scales: torch.Tensor, w_biases: torch.Tensor,
+                  y: torch.Tensor, GS: int, bits: int, stream=None) -> torch.Tensor:
+    """y[t, n] = sum_k x[t, k] * (scale * code + bias)[n, k]: x ``[T, K]`` bf16/fp16, packed ``[N, K*bits/32]``,
+    scales/biases ``[N, K/GS]`` in x's dtype, y ``[T, N]`` (bf16, fp16 or fp32)."""
+    T, K = x.shape
+    N = w_packed.shape[0]
+    st = lib().qdecode_qgemv(_ptr(x), _ptr(w_packed), _ptr(w_scales), _ptr(w_biases), _ptr(y), T, N, K, GS, bits,
+                             dtype_code(x.dtype, y.dtype), _stream(stream))
+    _lib.check(st, "qdecode_qgemv")
+    return y
+
+
 def qdecode_attn_device_status() -> int:
     flags = ctypes.c_uint()
     _lib.check(lib().qdecode_attn_device_status(ctypes.byref(flags)), "qdecode_attn_device_status")

@@ -20,6 +20,7 @@ QDA_BF16, QDA_FP16, QDA_FP32 = 1, 2, 3
 QDA_MAX_B = 512
 QDA_MAX_NREP = 64
 QDA_MAX_L = 8
+QDA_QGEMV_MAX_T = 4
 
 
 class QdaPlan(ctypes.Structure):
@@ -55,6 +56,7 @@ SIGNATURES = {
     "qdecode_attn_set_workspace": (_I, [_P, _SZ]),
     "qdecode_attn_debug_force_splits": (_I, [_I]),
     "qdecode_attn_set_split_event": (_I, [_P]),
+    "qdecode_qgemv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "qdecode_quantize": (_I, [_P, _LL, _I, _I, _I, _I, _P, _P, _P, _P]),
     "qdecode_attn_strerror": (ctypes.c_char_p, [_I]),
     "qdecode_attn_last_cuda_error": (_I, []),

@@ -104,6 +104,9 @@ cudaError_t qda_occupancy_split2_b4_x1(int D, int nh, int ng, size_t smem, int* 
 cudaError_t qda_occupancy_split2_b8_x0(int D, int nh, int ng, size_t smem, int* ctas_per_sm);
 cudaError_t qda_occupancy_split2_b8_x1(int D, int nh, int ng, size_t smem, int* ctas_per_sm);
 
+// Records a CUDA runtime error for qdecode_attn_last_cuda_error() (this host thread) and returns QDA_ERR_CUDA.
+int qda_cuda_fail(cudaError_t e);
+
 cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool pdl, cudaStream_t s);
 
 cudaError_t qda_launch_quantize(const float* x, long long rows, int D, int GS, int bits, int in_dtype,

@@ -379,6 +379,8 @@ int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, cons
 
 }  // namespace
 
+int qda_cuda_fail(cudaError_t e) { return cuda_fail(e); }
+
 extern "C" {
 
 int qdecode_attn_plan(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int num_sms,

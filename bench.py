@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2)
-    ap.add_argument("--no-extra", action="store_true", help="skip the per-workload figures (workloads 3-5, 4-position multi-query decode, two-pass compat form)")
+    ap.add_argument("--no-extra", action="store_true", help="skip the per-workload figures (workloads 3-5, multi-query decode, two-pass compat form, 8-bit GEMV)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -375,6 +375,24 @@ def run_ours(args):
                 "us_per_call": round(mc * 1e3, 2), "kv_GBps": round(nbytes / (mc * 1e-3) / 1e9, 1),
                 "frac_of_peak": round(nbytes / (mc * 1e-3) / 1e9 / peak, 4), "kv_bytes": nbytes,
                 "note": "K is read in both passes; kv_GBps counts each KV byte once"}
+        # the codec under a plain GEMV: an MLP-sized 8-bit matrix (K = 4096, N = 14336, GS = 64) times one vector;
+        # random codes, scales and biases (the kernel's time does not depend on their values)
+        gK, gN, gGS = 4096, 14336, 64
+        gen = torch.Generator(device=device).manual_seed(20261202)
+        gw = torch.randint(-2 ** 31, 2 ** 31 - 1, (gN, gK // 4), generator=gen, device=device, dtype=torch.int32)
+        gs = (torch.rand(gN, gK // gGS, generator=gen, device=device) * 0.02).to(torch.bfloat16)
+        gb = (torch.randn(gN, gK // gGS, generator=gen, device=device)).to(torch.bfloat16)
+        gx = torch.randn(1, gK, generator=gen, device=device).to(torch.bfloat16)
+        gy = torch.empty(1, gN, dtype=torch.float32, device=device)
+        gcall = lambda: qda.qdecode_qgemv(gx, gw, gs, gb, gy, gGS, 8, stream)
+        for _ in range(5):
+            gcall()
+        mg = statistics.median(time_calls(gcall, 50, flush, stream))
+        gbytes = gN * gK + 2 * 2 * gN * (gK // gGS)
+        extra["qgemv_8b_K4096_N14336_T1_GS64_bf16"] = {
+            "us_per_call": round(mg * 1e3, 2), "GBps": round(gbytes / (mg * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(gbytes / (mg * 1e-3) / 1e9 / peak, 4), "weight_bytes": gbytes}
+        del gw, gs, gb, gx, gy
         # small-L multi-query decode on this workload's cache: 4 query positions (the last 4 tokens) per sequence
         Lq = 4
         qm = synth.query_multi(w, Lq).to(device)

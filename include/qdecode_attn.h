@@ -193,6 +193,21 @@ int qdecode_attn_set_split_event(void* event);
 int qdecode_quantize(const float* x, long long rows, int D, int GS, int bits, int dtype, uint32_t* packed,
                      void* scales, void* biases, void* stream);
 
+/*
+ * qdecode_qgemv: the cache's affine codec under a plain matrix-vector product, a comparison workload (maya-mac
+ * mlx_kernels.py, _linear_kernel: weights dequantised inline as code * scale + bias per group of GS along a row):
+ *
+ *     y[t, n] = sum_k x[t, k] * (scale[n, k / GS] * code[n, k] + bias[n, k / GS]),   0 <= t < T
+ *
+ * x [T, K] and the scales and biases in the input dtype of `dtype` (bf16 or fp16); packed [N, K * bits / 32] uint32,
+ * codes least-significant first; scales, biases [N, K / GS]; y [T, N] in the output dtype (as for qdecode_attn:
+ * 0 = the input dtype). Asynchronous on `stream`, no workspace. Requires bits in {4, 8}, GS in {32, 64, 128},
+ * 1 <= T <= QDA_QGEMV_MAX_T and K a multiple of 512 (else QDA_ERR_UNSUPPORTED); pointers 16-byte aligned.
+ */
+#define QDA_QGEMV_MAX_T 4
+int qdecode_qgemv(const void* x, const uint32_t* w_packed, const void* w_scales, const void* w_biases, void* y,
+                  int T, int N, int K, int GS, int bits, int dtype, void* stream);
+
 /* Human-readable text for a status code (static storage). */
 const char* qdecode_attn_strerror(int status);
 

@@ -239,3 +239,19 @@ def test_compat_argument_errors(L):
     q = list(p)
     q[2] = None
     assert L.qdecode_attn_compat(*q, 1, 8, 2, n, 256, 32, 4, 1, None) == _lib.QDA_ERR_INVALID
+
+
+def test_qgemv_argument_errors(L):
+    g = L.qdecode_qgemv
+    p = [FAKE + 256 * i for i in range(5)]
+    assert g(None, *p[1:], 1, 64, 1024, 64, 8, 1, None) == _lib.QDA_ERR_INVALID
+    assert g(*p, 0, 64, 1024, 64, 8, 1, None) == _lib.QDA_ERR_INVALID
+    assert g(*p, 1, 0, 1024, 64, 8, 1, None) == _lib.QDA_ERR_INVALID
+    assert g(*p, 5, 64, 1024, 64, 8, 1, None) == _lib.QDA_ERR_UNSUPPORTED      # T > QDA_QGEMV_MAX_T
+    assert g(*p, 1, 64, 1000, 8, 8, 1, None) == _lib.QDA_ERR_UNSUPPORTED       # GS
+    assert g(*p, 1, 64, 1280, 64, 8, 1, None) == _lib.QDA_ERR_UNSUPPORTED      # K not a multiple of 512
+    assert g(*p, 1, 64, 1024, 64, 2, 1, None) == _lib.QDA_ERR_UNSUPPORTED
+    assert g(*p, 1, 64, 1024, 64, 8, 3, None) == _lib.QDA_ERR_INVALID          # fp32 input
+    q = list(p)
+    q[4] += 4
+    assert g(*q, 1, 64, 1024, 64, 8, 1, None) == _lib.QDA_ERR_ALIGN
