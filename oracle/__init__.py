@@ -10,6 +10,7 @@ from .qda_oracle import (  # noqa: F401
     attention_head_compat,
     attention_packed_compat,
     attention_two_pass_blocked,
+    cache_append,
     attention_head,
     attention_packed,
     attention_packed_multi,

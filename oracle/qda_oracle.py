@@ -24,6 +24,7 @@ What it computes, step by step, in the order of the method's description:
 7. ``attention_head_compat`` / ``attention_two_pass_blocked`` / ``attention_packed_compat``: the two-pass variant
    with the pages' compat rounding points (scores and normalised probabilities rounded to the input dtype T).
 8. ``qgemv``: the same affine codec under a plain matrix-vector product (a comparison workload).
+9. ``cache_append``: the step before decode: every KV head's old rows, then the new tokens' rows quantized.
 
 Readings taken where the pages are silent (each pinned by a test in ``tests/test_oracle.py``):
 
@@ -329,6 +330,30 @@ def attention_packed_compat(q, kp, ks, kb, vp, vs, vb, N, H: int, Hkv: int, D: i
         Kd, Vd = cache[key]
         res[(b, h)] = attention_head_compat(q[b, h], Kd, Vd, dtype)
     return res
+
+
+def cache_append(old, N, K_new, V_new, Hkv: int, D: int, GS: int, bits: int, dtype: str):
+    """Append T new tokens per sequence to a packed cache (maya-mac ``mlx_kernels.py``, ``_ATTEND``: each pass writes
+    the cache anew, every KV head's old rows followed by this pass's new rows).
+
+    old: (kp, ks, kb, vp, vs, vb) in the back-to-back layout for lengths N; K_new, V_new ``[B, Hkv, T, D]`` fp32.
+    Returns the six arrays for lengths N[b] + T: per (b, kvh) the old rows unchanged, then the new rows quantized.
+    """
+    K_new = np.asarray(K_new, np.float32)
+    V_new = np.asarray(V_new, np.float32)
+    B, _, T, _ = K_new.shape
+    kn = quantize_cache(K_new.reshape(-1, D), V_new.reshape(-1, D), GS, bits, dtype)
+    parts = [[] for _ in range(6)]
+    r_old = 0
+    for b in range(B):
+        n = int(N[b])
+        for kvh in range(Hkv):
+            i_new = (b * Hkv + kvh) * T
+            for a in range(6):
+                parts[a].append(np.asarray(old[a])[r_old:r_old + n])
+                parts[a].append(kn[a][i_new:i_new + T])
+            r_old += n
+    return tuple(np.concatenate(p) for p in parts)
 
 
 def qgemv(x, wp, ws, wb, K: int, GS: int, bits: int) -> np.ndarray:

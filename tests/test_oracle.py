@@ -475,3 +475,49 @@ def test_qgemv_brute_force_loops(bits):
         for n in range(N):
             ref = sum(float(x[t, k]) * (float(c[n, k]) * float(s[n, k // GS]) + float(b[n, k // GS])) for k in range(K))
             assert abs(y[t, n] - ref) <= 1e-12 * max(1.0, abs(ref))
+
+
+# ------------------------------------------------------------------------------------ appending to the cache
+
+
+@pytest.mark.parametrize("bits,GS,dtype", [(4, 32, "bf16"), (8, 64, "fp16"), (4, 128, "fp16")])
+def test_cache_append_equals_quantizing_the_longer_cache(bits, GS, dtype):
+    # the quantizer works row by row, so appending quantized rows equals quantizing the concatenated rows
+    rng = np.random.default_rng(51 + bits)
+    N, Hkv, T, D = [5, 0, 12], 2, 3, 128
+    B = len(N)
+    old_k = [rng.standard_normal((Hkv, n, D)).astype(np.float32) for n in N]
+    old_v = [rng.standard_normal((Hkv, n, D)).astype(np.float32) for n in N]
+    Kn = rng.standard_normal((B, Hkv, T, D)).astype(np.float32)
+    Vn = rng.standard_normal((B, Hkv, T, D)).astype(np.float32)
+    flat = lambda xs: np.concatenate([x.reshape(-1, D) for x in xs])
+    old = O.quantize_cache(flat(old_k), flat(old_v), GS, bits, dtype)
+    got = O.cache_append(old, N, Kn, Vn, Hkv, D, GS, bits, dtype)
+    long_k = [np.concatenate([old_k[b], Kn[b]], axis=1) for b in range(B)]
+    long_v = [np.concatenate([old_v[b], Vn[b]], axis=1) for b in range(B)]
+    ref = O.quantize_cache(flat(long_k), flat(long_v), GS, bits, dtype)
+    for g, r in zip(got, ref):
+        np.testing.assert_array_equal(g, r)
+
+
+def test_cache_append_attention_sees_the_new_rows():
+    # decode over the appended cache with L = T query positions equals decode over the longer fp32 rows
+    rng = np.random.default_rng(52)
+    N, Hkv, T, D, GS, bits, H = [7, 3], 1, 2, 64, 32, 8, 2
+    B = len(N)
+    old_k = rng.standard_normal((sum(N) * Hkv, D)).astype(np.float32)
+    old_v = rng.standard_normal((sum(N) * Hkv, D)).astype(np.float32)
+    Kn = rng.standard_normal((B, Hkv, T, D)).astype(np.float32)
+    Vn = rng.standard_normal((B, Hkv, T, D)).astype(np.float32)
+    new = O.cache_append(O.quantize_cache(old_k, old_v, GS, bits, "bf16"), N, Kn, Vn, Hkv, D, GS, bits, "bf16")
+    N2 = [n + T for n in N]
+    q = rng.standard_normal((B, T, H, D))
+    out = O.attention_packed_multi(q, *new, N2, T, H, Hkv, D, GS, bits)
+    kp, ks, kb, vp, vs, vb = new
+    for b in range(B):
+        r0, r1 = O.unit_rows(N2, Hkv, b, 0)
+        Kd = O.dequantize(O.unpack(kp[r0:r1], bits, D), ks[r0:r1], kb[r0:r1], GS)
+        Vd = O.dequantize(O.unpack(vp[r0:r1], bits, D), vs[r0:r1], vb[r0:r1], GS)
+        for t in range(T):
+            for h in range(H):
+                np.testing.assert_array_equal(out[(b, t, h)], O.attention_head(q[b, t, h], Kd[:N[b] + 1 + t], Vd[:N[b] + 1 + t]))
