@@ -223,6 +223,22 @@ class QuantizedKV:
     def nbytes(self) -> int:
         return sum(t.numel() * t.element_size() for t in (self.kp, self.ks, self.kb, self.vp, self.vs, self.vb))
 
+    def append(self, K_new: torch.Tensor, V_new: torch.Tensor, out: "QuantizedKV" = None, stream=None) -> "QuantizedKV":
+        """The cache with T new tokens per sequence (``K_new``, ``V_new`` fp32 ``[B, Hkv, T, D]``): every KV head's
+        old rows, then the new rows quantized (qdecode_cache_append). Writes ``out`` (allocated when None)."""
+        B, Hkv, T, D = K_new.shape
+        kn, vn = K_new.contiguous(), V_new.contiguous()
+        if out is None:
+            out = QuantizedKV.empty([n + T for n in self.N], self.Hkv, self.D, self.GS, self.bits, self.dtype,
+                                    device=K_new.device)
+        st = lib().qdecode_cache_append(
+            _ptr(self.kp), _ptr(self.ks), _ptr(self.kb), _ptr(self.vp), _ptr(self.vs), _ptr(self.vb),
+            _ptr(kn), _ptr(vn), _ptr(out.kp), _ptr(out.ks), _ptr(out.kb),
+            _ptr(out.vp), _ptr(out.vs), _ptr(out.vb), B, Hkv, _lib.int32_array(self.N), T, D, self.GS, self.bits,
+            dtype_code(self.dtype), _stream(stream))
+        _lib.check(st, "qdecode_cache_append")
+        return out
+
 
 def bind_decode_attention(q: torch.Tensor, cache: QuantizedKV, out: torch.Tensor, stream=None):
     """Pre-marshalled decode_attention over a QuantizedKV (see bind_qdecode_attn)."""

@@ -57,6 +57,7 @@ SIGNATURES = {
     "qdecode_attn_debug_force_splits": (_I, [_I]),
     "qdecode_attn_set_split_event": (_I, [_P]),
     "qdecode_qgemv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "qdecode_cache_append": (_I, [_P] * 14 + [_I, _I, _PI32, _I, _I, _I, _I, _I, _P]),
     "qdecode_quantize": (_I, [_P, _LL, _I, _I, _I, _I, _P, _P, _P, _P]),
     "qdecode_attn_strerror": (ctypes.c_char_p, [_I]),
     "qdecode_attn_last_cuda_error": (_I, []),

@@ -109,5 +109,23 @@ int qda_cuda_fail(cudaError_t e);
 
 cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool pdl, cudaStream_t s);
 
+// Where the quantizer writes its rows. append = 0: row i to row i. append = 1 (cache append): input row
+// i = ((b * Hkv) + kvh) * T + t goes to row Hkv * off_new[b] + kvh * (n_old[b] + T) + n_old[b] + t of the new cache,
+// off_new[b] = sum over earlier sequences of n_old + T; off_old is the old cache's sequence starts (sum of n_old).
+struct QdaRowMap {
+  int append, B, Hkv, T;
+  int n_old[QDA_MAX_B];
+  int off_old[QDA_MAX_B + 1];
+  int off_new[QDA_MAX_B + 1];
+};
+
 cudaError_t qda_launch_quantize(const float* x, long long rows, int D, int GS, int bits, int in_dtype,
-                                uint32_t* packed, uint16_t* scales, uint16_t* biases, cudaStream_t s);
+                                uint32_t* packed, uint16_t* scales, uint16_t* biases, cudaStream_t s,
+                                const QdaRowMap* map = nullptr);
+
+// Copies every old row of a cache into its place in the appended cache (map->append = 1); W words and NG scales
+// and biases per row, for K and V.
+cudaError_t qda_launch_append_copy(const uint32_t* kp, const uint16_t* ks, const uint16_t* kb, const uint32_t* vp,
+                                   const uint16_t* vs, const uint16_t* vb, uint32_t* kpo, uint16_t* kso,
+                                   uint16_t* kbo, uint32_t* vpo, uint16_t* vso, uint16_t* vbo, long long rows_old,
+                                   int W, int NG, const QdaRowMap& map, cudaStream_t s);

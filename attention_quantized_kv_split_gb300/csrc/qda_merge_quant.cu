@@ -128,10 +128,19 @@ __device__ __forceinline__ uint32_t round_bits16(float x) {
 }
 
 // One warp per row of D = 32 * E fp32 values; lane l holds elements [l*E, l*E + E). A group spans GS/E lanes.
+__device__ __forceinline__ long long mapped_row(const QdaRowMap& m, long long i) {
+  if (!m.append) return i;
+  const int per_seq = m.Hkv * m.T;
+  const int b = (int)(i / per_seq);
+  const int rem = (int)(i - (long long)b * per_seq);
+  const int kvh = rem / m.T, t = rem - kvh * m.T;
+  return (long long)m.Hkv * m.off_new[b] + (long long)kvh * (m.n_old[b] + m.T) + m.n_old[b] + t;
+}
+
 template <int BITS, int E, bool F16>
 __global__ void __launch_bounds__(256) qda_quant_kernel(const float* __restrict__ x, long long rows, int GS,
                                                         uint32_t* __restrict__ packed, uint16_t* __restrict__ sc,
-                                                        uint16_t* __restrict__ bi) {
+                                                        uint16_t* __restrict__ bi, const __grid_constant__ QdaRowMap map) {
   constexpr int D = 32 * E;
   constexpr int PER = 32 / BITS;
   constexpr int W = D / PER;
@@ -140,6 +149,7 @@ __global__ void __launch_bounds__(256) qda_quant_kernel(const float* __restrict_
   if (row >= rows) return;
   const int lane = threadIdx.x & 31;
   const float* xr = x + row * D + lane * E;
+  const long long orow = mapped_row(map, row);   // the row written
   float v[E];
   if constexpr (E % 4 == 0) {
 #pragma unroll
@@ -188,7 +198,7 @@ __global__ void __launch_bounds__(256) qda_quant_kernel(const float* __restrict_
       uint32_t word = 0;
 #pragma unroll
       for (int k = 0; k < PER; ++k) word |= code[w * PER + k] << (BITS * k);
-      packed[row * W + lane * WL + w] = word;
+      packed[orow * W + lane * WL + w] = word;
     }
   } else {
     constexpr int LPW = 32 / (E * BITS);  // lanes sharing a word
@@ -198,24 +208,57 @@ __global__ void __launch_bounds__(256) qda_quant_kernel(const float* __restrict_
     part <<= (E * BITS) * (lane % LPW);
 #pragma unroll
     for (int off = 1; off < LPW; off <<= 1) part |= __shfl_xor_sync(0xffffffffu, part, off);
-    if (lane % LPW == 0) packed[row * W + lane / LPW] = part;
+    if (lane % LPW == 0) packed[orow * W + lane / LPW] = part;
   }
   if ((lane * E) % GS == 0) {
     const int NG = D / GS;
-    sc[row * NG + (lane * E) / GS] = (uint16_t)sbits;
-    bi[row * NG + (lane * E) / GS] = (uint16_t)bbits;
+    sc[orow * NG + (lane * E) / GS] = (uint16_t)sbits;
+    bi[orow * NG + (lane * E) / GS] = (uint16_t)bbits;
+  }
+}
+
+// One warp per old row: its K and V words, scales and biases move to the row's place in the appended cache
+// (every KV head's block grows by T rows, so rows shift by the new rows of the blocks before them).
+__global__ void __launch_bounds__(256) qda_append_copy_kernel(
+    const uint32_t* __restrict__ kp, const uint16_t* __restrict__ ks, const uint16_t* __restrict__ kb,
+    const uint32_t* __restrict__ vp, const uint16_t* __restrict__ vs, const uint16_t* __restrict__ vb,
+    uint32_t* __restrict__ kpo, uint16_t* __restrict__ kso, uint16_t* __restrict__ kbo, uint32_t* __restrict__ vpo,
+    uint16_t* __restrict__ vso, uint16_t* __restrict__ vbo, long long rows_old, int W, int NG,
+    const __grid_constant__ QdaRowMap m) {
+  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows_old) return;
+  const int lane = threadIdx.x & 31;
+  int lo = 0, hi = m.B - 1;   // the last sequence whose old rows start at or before this row (skips empty ones)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)m.Hkv * m.off_old[mid] <= row) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const long long local = row - (long long)m.Hkv * m.off_old[b];
+  const int kvh = (int)(local / m.n_old[b]);
+  const long long j = local - (long long)kvh * m.n_old[b];
+  const long long dst = (long long)m.Hkv * m.off_new[b] + (long long)kvh * (m.n_old[b] + m.T) + j;
+  for (int w = lane; w < W; w += 32) {
+    kpo[dst * W + w] = kp[row * W + w];
+    vpo[dst * W + w] = vp[row * W + w];
+  }
+  for (int g = lane; g < NG; g += 32) {
+    kso[dst * NG + g] = ks[row * NG + g];
+    kbo[dst * NG + g] = kb[row * NG + g];
+    vso[dst * NG + g] = vs[row * NG + g];
+    vbo[dst * NG + g] = vb[row * NG + g];
   }
 }
 
 template <int BITS, bool F16>
 cudaError_t launch_quant(const float* x, long long rows, int D, int GS, uint32_t* packed, uint16_t* sc, uint16_t* bi,
-                         cudaStream_t s) {
+                         cudaStream_t s, const QdaRowMap& m) {
   const unsigned blocks = (unsigned)((rows + 7) / 8);
   switch (D) {
-    case 64: qda_quant_kernel<BITS, 2, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi); break;
-    case 128: qda_quant_kernel<BITS, 4, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi); break;
-    case 256: qda_quant_kernel<BITS, 8, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi); break;
-    case 512: qda_quant_kernel<BITS, 16, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi); break;
+    case 64: qda_quant_kernel<BITS, 2, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi, m); break;
+    case 128: qda_quant_kernel<BITS, 4, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi, m); break;
+    case 256: qda_quant_kernel<BITS, 8, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi, m); break;
+    case 512: qda_quant_kernel<BITS, 16, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi, m); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -243,12 +286,26 @@ cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool 
 }
 
 cudaError_t qda_launch_quantize(const float* x, long long rows, int D, int GS, int bits, int in_dtype,
-                                uint32_t* packed, uint16_t* scales, uint16_t* biases, cudaStream_t s) {
+                                uint32_t* packed, uint16_t* scales, uint16_t* biases, cudaStream_t s,
+                                const QdaRowMap* map) {
+  static const QdaRowMap kIdentity = {};
+  const QdaRowMap& m = map ? *map : kIdentity;
   const bool f16 = in_dtype == QDA_FP16;
   if (bits == 4) {
-    return f16 ? qda::launch_quant<4, true>(x, rows, D, GS, packed, scales, biases, s)
-               : qda::launch_quant<4, false>(x, rows, D, GS, packed, scales, biases, s);
+    return f16 ? qda::launch_quant<4, true>(x, rows, D, GS, packed, scales, biases, s, m)
+               : qda::launch_quant<4, false>(x, rows, D, GS, packed, scales, biases, s, m);
   }
-  return f16 ? qda::launch_quant<8, true>(x, rows, D, GS, packed, scales, biases, s)
-             : qda::launch_quant<8, false>(x, rows, D, GS, packed, scales, biases, s);
+  return f16 ? qda::launch_quant<8, true>(x, rows, D, GS, packed, scales, biases, s, m)
+             : qda::launch_quant<8, false>(x, rows, D, GS, packed, scales, biases, s, m);
+}
+
+cudaError_t qda_launch_append_copy(const uint32_t* kp, const uint16_t* ks, const uint16_t* kb, const uint32_t* vp,
+                                   const uint16_t* vs, const uint16_t* vb, uint32_t* kpo, uint16_t* kso,
+                                   uint16_t* kbo, uint32_t* vpo, uint16_t* vso, uint16_t* vbo, long long rows_old,
+                                   int W, int NG, const QdaRowMap& map, cudaStream_t s) {
+  if (rows_old <= 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((rows_old + 7) / 8);
+  qda::qda_append_copy_kernel<<<blocks, 256, 0, s>>>(kp, ks, kb, vp, vs, vb, kpo, kso, kbo, vpo, vso, vbo, rows_old,
+                                                     W, NG, map);
+  return cudaGetLastError();
 }

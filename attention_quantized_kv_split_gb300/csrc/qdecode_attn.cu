@@ -473,6 +473,64 @@ int qdecode_quantize(const float* x, long long rows, int D, int GS, int bits, in
   return QDA_OK;
 }
 
+int qdecode_cache_append(const uint32_t* k_packed, const void* k_scales, const void* k_biases,
+                         const uint32_t* v_packed, const void* v_scales, const void* v_biases, const float* k_new,
+                         const float* v_new, uint32_t* k_packed_out, void* k_scales_out, void* k_biases_out,
+                         uint32_t* v_packed_out, void* v_scales_out, void* v_biases_out, int B, int Hkv,
+                         const int32_t* N, int T, int D, int GS, int bits, int dtype, void* stream) {
+  if (!k_new || !v_new || !k_packed_out || !k_scales_out || !k_biases_out || !v_packed_out || !v_scales_out ||
+      !v_biases_out || N == nullptr)
+    return QDA_ERR_INVALID;
+  if (B < 1 || Hkv < 1 || T < 1 || D < 1 || GS < 1) return QDA_ERR_INVALID;
+  int in_dt, out_dt;
+  int st = check_dtype(dtype, &in_dt, &out_dt);
+  if (st != QDA_OK) return st;
+  if (bits != 4 && bits != 8) return QDA_ERR_UNSUPPORTED;
+  if (GS != 32 && GS != 64 && GS != 128) return QDA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256 && D != 512) return QDA_ERR_UNSUPPORTED;
+  if (D % GS != 0 || B > QDA_MAX_B) return QDA_ERR_UNSUPPORTED;
+  long long total_old = 0;
+  for (int b = 0; b < B; ++b) {
+    if (N[b] < 0) return QDA_ERR_INVALID;
+    total_old += N[b];
+  }
+  if (total_old + (long long)B * T > (1LL << 31) - 1) return QDA_ERR_UNSUPPORTED;   // sequence offsets are int32
+  if (total_old > 0 && (!k_packed || !k_scales || !k_biases || !v_packed || !v_scales || !v_biases))
+    return QDA_ERR_INVALID;
+  const void* ptrs[10] = {k_new, v_new, k_packed_out, k_scales_out, k_biases_out, v_packed_out, v_scales_out,
+                          v_biases_out, k_packed, v_packed};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return QDA_ERR_ALIGN;
+  QdaRowMap m;
+  std::memset(&m, 0, sizeof(m));
+  m.append = 1;
+  m.B = B;
+  m.Hkv = Hkv;
+  m.T = T;
+  for (int b = 0; b < B; ++b) {
+    m.n_old[b] = N[b];
+    m.off_old[b + 1] = m.off_old[b] + N[b];
+    m.off_new[b + 1] = m.off_new[b] + N[b] + T;
+  }
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int W = D * bits / 32, NG = D / GS;
+  cudaError_t e = qda_launch_append_copy(
+      k_packed, static_cast<const uint16_t*>(k_scales), static_cast<const uint16_t*>(k_biases), v_packed,
+      static_cast<const uint16_t*>(v_scales), static_cast<const uint16_t*>(v_biases), k_packed_out,
+      static_cast<uint16_t*>(k_scales_out), static_cast<uint16_t*>(k_biases_out), v_packed_out,
+      static_cast<uint16_t*>(v_scales_out), static_cast<uint16_t*>(v_biases_out), (long long)Hkv * total_old, W, NG,
+      m, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const long long rows_new = (long long)B * Hkv * T;
+  e = qda_launch_quantize(k_new, rows_new, D, GS, bits, in_dt, k_packed_out, static_cast<uint16_t*>(k_scales_out),
+                          static_cast<uint16_t*>(k_biases_out), s, &m);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = qda_launch_quantize(v_new, rows_new, D, GS, bits, in_dt, v_packed_out, static_cast<uint16_t*>(v_scales_out),
+                          static_cast<uint16_t*>(v_biases_out), s, &m);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return QDA_OK;
+}
+
 const char* qdecode_attn_strerror(int status) {
   switch (status) {
     case QDA_OK: return "success";

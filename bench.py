@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2)
-    ap.add_argument("--no-extra", action="store_true", help="skip the per-workload figures (workloads 3-5, multi-query decode, two-pass compat form, 8-bit GEMV)")
+    ap.add_argument("--no-extra", action="store_true", help="skip the per-workload figures (workloads 3-5, multi-query decode, two-pass compat form, 8-bit GEMV, cache append)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -393,6 +393,19 @@ def run_ours(args):
             "us_per_call": round(mg * 1e3, 2), "GBps": round(gbytes / (mg * 1e-3) / 1e9, 1),
             "frac_of_peak": round(gbytes / (mg * 1e-3) / 1e9 / peak, 4), "weight_bytes": gbytes}
         del gw, gs, gb, gx, gy
+        # the step before decode: the next cache, this one's rows plus one new token per (sequence, KV head)
+        akn = torch.randn(w.B, w.Hkv, 1, w.D, generator=gen, device=device)
+        avn = torch.randn(w.B, w.Hkv, 1, w.D, generator=gen, device=device)
+        anext = qda.QuantizedKV.empty([n + 1 for n in N], w.Hkv, w.D, w.GS, w.bits, synth.DT[w.dtype_in], device=device)
+        acall = lambda: cache.append(akn, avn, out=anext, stream=stream)
+        for _ in range(5):
+            acall()
+        ma = statistics.median(time_calls(acall, 50, flush, stream))
+        abytes = nbytes + anext.nbytes()   # old cache read once, new cache written once
+        extra[f"{w.name}_append_1_token"] = {
+            "us_per_call": round(ma * 1e3, 2), "GBps": round(abytes / (ma * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(abytes / (ma * 1e-3) / 1e9 / peak, 4), "bytes_moved": abytes}
+        del akn, avn, anext
         # small-L multi-query decode on this workload's cache: 4 query positions (the last 4 tokens) per sequence
         Lq = 4
         qm = synth.query_multi(w, Lq).to(device)

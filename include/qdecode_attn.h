@@ -208,6 +208,21 @@ int qdecode_quantize(const float* x, long long rows, int D, int GS, int bits, in
 int qdecode_qgemv(const void* x, const uint32_t* w_packed, const void* w_scales, const void* w_biases, void* y,
                   int T, int N, int K, int GS, int bits, int dtype, void* stream);
 
+/*
+ * qdecode_cache_append: the cache for the next step, with T new tokens per sequence (maya-mac mlx_kernels.py,
+ * _ATTEND: each pass writes the cache anew, every KV head's old rows followed by the pass's new rows). Reads the
+ * cache for lengths N[b] (N[b] >= 0; with every N[b] = 0 the six old pointers may be NULL) and k_new, v_new
+ * [B, Hkv, T, D] fp32 (device); writes the six *_out arrays in the same back-to-back layout for lengths N[b] + T:
+ * per (b, kvh) the old rows copied unchanged, then the new rows quantized exactly as qdecode_quantize does (so the
+ * result equals quantizing the longer fp32 cache). The output must not overlap the input. Same dtype argument,
+ * shapes and errors as qdecode_quantize (plus B <= QDA_MAX_B); pointers 16-byte aligned. Asynchronous on stream.
+ */
+int qdecode_cache_append(const uint32_t* k_packed, const void* k_scales, const void* k_biases,
+                         const uint32_t* v_packed, const void* v_scales, const void* v_biases, const float* k_new,
+                         const float* v_new, uint32_t* k_packed_out, void* k_scales_out, void* k_biases_out,
+                         uint32_t* v_packed_out, void* v_scales_out, void* v_biases_out, int B, int Hkv,
+                         const int32_t* N, int T, int D, int GS, int bits, int dtype, void* stream);
+
 /* Human-readable text for a status code (static storage). */
 const char* qdecode_attn_strerror(int status);
 

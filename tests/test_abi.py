@@ -255,3 +255,23 @@ def test_qgemv_argument_errors(L):
     q = list(p)
     q[4] += 4
     assert g(*q, 1, 64, 1024, 64, 8, 1, None) == _lib.QDA_ERR_ALIGN
+
+
+def test_cache_append_argument_errors(L):
+    a = L.qdecode_cache_append
+    old = [FAKE + 256 * i for i in range(6)]
+    new = [FAKE + 4096, FAKE + 8192]
+    out = [FAKE + 16384 + 256 * i for i in range(6)]
+    n = _lib.int32_array([5, 0])
+    def call(B=2, Hkv=2, nn=n, T=1, D=256, GS=64, bits=4, dtype=1, o=old, w=new, x=out):
+        return a(*o, *w, *x, B, Hkv, nn, T, D, GS, bits, dtype, None)
+    assert call(T=0) == _lib.QDA_ERR_INVALID
+    assert call(Hkv=0) == _lib.QDA_ERR_INVALID
+    assert call(nn=_lib.int32_array([5, -1])) == _lib.QDA_ERR_INVALID
+    assert call(nn=None) == _lib.QDA_ERR_INVALID
+    assert call(D=96, GS=32) == _lib.QDA_ERR_UNSUPPORTED
+    assert call(bits=3) == _lib.QDA_ERR_UNSUPPORTED
+    assert call(dtype=3) == _lib.QDA_ERR_INVALID
+    assert call(o=[None] * 6) == _lib.QDA_ERR_INVALID             # old rows exist but no old cache
+    assert call(x=[None] + out[1:]) == _lib.QDA_ERR_INVALID
+    assert call(w=[new[0] + 4, new[1]]) == _lib.QDA_ERR_ALIGN
