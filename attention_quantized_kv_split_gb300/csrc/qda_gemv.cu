@@ -4,12 +4,15 @@
 // striding along K, dequantisation inlined; its LayerNorm, activation and residual epilogues are model-specific and
 // not part of this workload).
 //
-// One warp owns R = 4 output rows; each step a lane takes 16 consecutive elements of K (one 16- or 8-byte load
-// per row, streamed past L1), the x slice of those elements (read through the read-only path: every warp of the
-// GPU reads the same few KB of x), and the row's scale and bias of that group. The dot is factored as in the
-// attention kernels: s * sum(x * code) + b * sum(x), with exact codes (2^23 + code minus 2^23) and packed f32x2
-// FMAs. Lanes then reduce by shuffles and lane 0 writes the rounded outputs. A warp-per-row-group GEMV streams the
-// weights once with no shared memory, which is all a matrix-vector product needs: it is bound by HBM.
+// S warps own R = 4 output rows, each taking 1/S of K (S = 1, 2 or 4, chosen so that a wide matrix still spreads
+// over every SM); each step a lane takes 128 bits of codes (16 elements of 8-bit, 32 of 4-bit) per row, streamed
+// past L1, the x slice of those elements (read through the read-only path: every warp reads the same few KB of x),
+// and the row's scale and bias of that group. The dot is factored as in the attention kernels: s * sum(x * code) +
+// b * sum(x), with exact codes (2^23 + code minus 2^23) and packed f32x2 FMAs. Lanes reduce by shuffles, the S
+// parts meet in shared memory in a fixed order, and one lane writes the rounded outputs. The weights are streamed
+// once: a matrix-vector product is bound by HBM.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -20,30 +23,20 @@ namespace qda {
 
 constexpr int kGemvThreads = 256;
 constexpr int kGemvRows = 4;      // output rows per warp
-constexpr int kGemvCodes = 16;    // elements of K per lane per step
+constexpr int kGemvWarps = kGemvThreads / 32;
 
+// elements of K per lane per step: one 128-bit load of codes
 template <int BITS>
-__device__ __forceinline__ void load_codes(const uint32_t* p, uint32_t (&w)[kGemvCodes * BITS / 32]) {
-  if constexpr (BITS == 8) {
-    const uint4 v = __ldcs(reinterpret_cast<const uint4*>(p));
-    w[0] = v.x;
-    w[1] = v.y;
-    w[2] = v.z;
-    w[3] = v.w;
-  } else {
-    const uint2 v = __ldcs(reinterpret_cast<const uint2*>(p));
-    w[0] = v.x;
-    w[1] = v.y;
-  }
-}
+__host__ __device__ constexpr int gemv_codes() { return 128 / BITS; }
 
-// codes of the words as exact floats, in element order
+// codes of one 128-bit load as exact floats, in element order
 template <int BITS>
-__device__ __forceinline__ void codes_to_float(const uint32_t (&w)[kGemvCodes * BITS / 32], float (&c)[kGemvCodes]) {
+__device__ __forceinline__ void codes_to_float(const uint4 v, float (&c)[128 / BITS]) {
   constexpr int PER = 32 / BITS;
   constexpr uint32_t MASK = (1u << BITS) - 1u;
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int i = 0; i < kGemvCodes * BITS / 32; ++i)
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int k = 0; k < PER; ++k)
       c[i * PER + k] = __uint_as_float(0x4B000000u | ((w[i] >> (BITS * k)) & MASK)) - 8388608.0f;
@@ -60,98 +53,153 @@ __device__ __forceinline__ void store_out(void* y, size_t idx, float v) {
   }
 }
 
+// resident CTAs per SM the register budget aims at: three for one input row, fewer as the accumulators grow
 template <int BITS, int T, int OUT>
-__global__ void __launch_bounds__(kGemvThreads) qda_qgemv_kernel(const uint16_t* __restrict__ x,
+__global__ void __launch_bounds__(kGemvThreads, T == 1 ? 3 : T == 2 ? 2 : 1) qda_qgemv_kernel(const uint16_t* __restrict__ x,
                                                                 const uint32_t* __restrict__ wp,
                                                                 const uint16_t* __restrict__ ws,
                                                                 const uint16_t* __restrict__ wb, void* __restrict__ y,
-                                                                int N, int K, int GS, int f16) {
-  constexpr int R = kGemvRows, C = kGemvCodes;
+                                                                int N, int K, int GS, int f16, int S) {
+  constexpr int R = kGemvRows, C = gemv_codes<BITS>();
+  __shared__ float part[kGemvWarps][R][T];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = (blockIdx.x * (kGemvThreads / 32) + warp) * R;
-  if (n0 >= N) return;
+  const int grp = warp / S, sp = warp - grp * S;       // row group within the CTA's block of rows, K part
+  const int kpart = K / S, kbeg = sp * kpart;
   const int W = K * BITS / 32, NG = K / GS;
-  float2 acc[R][T];
+  const int rows_per_block = (kGemvWarps / S) * R;
+  const int blocks = (N + rows_per_block - 1) / rows_per_block;
+  // a grid of whole waves (SMs x resident CTAs) takes the blocks of rows in turn
+  for (int blk = blockIdx.x; blk < blocks; blk += gridDim.x) {
+    const int n0 = blk * rows_per_block + grp * R;
+    float2 acc[R][T];
 #pragma unroll
-  for (int r = 0; r < R; ++r)
+    for (int r = 0; r < R; ++r)
 #pragma unroll
-    for (int t = 0; t < T; ++t) acc[r][t] = make_float2(0.f, 0.f);
-  float bacc[R][T];   // sum of bias * sum(x) per row and input
+      for (int t = 0; t < T; ++t) acc[r][t] = make_float2(0.f, 0.f);
+    float bacc[R][T];   // sum of bias * sum(x) per row and input
 #pragma unroll
-  for (int r = 0; r < R; ++r)
+    for (int r = 0; r < R; ++r)
 #pragma unroll
-    for (int t = 0; t < T; ++t) bacc[r][t] = 0.f;
+      for (int t = 0; t < T; ++t) bacc[r][t] = 0.f;
 
-  for (int k0 = lane * C; k0 < K; k0 += 32 * C) {
-    // the x slice of these 16 elements, and its sums
-    float2 xv[T][C / 2];
-    float xs[T];
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      const uint4* xp = reinterpret_cast<const uint4*>(x + (size_t)t * K + k0);
-      const uint4 a = __ldg(xp), b = __ldg(xp + 1);
-      const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      float sum = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        xv[t][i] = make_float2(half_bits_to_float_rt(u[i] & 0xFFFFu, f16 != 0),
-                               half_bits_to_float_rt(u[i] >> 16, f16 != 0));
-        sum += xv[t][i].x + xv[t][i].y;
-      }
-      xs[t] = sum;
-    }
-    const int g = k0 / GS;
+    // the codes of the R rows are loaded one step ahead (a register double buffer), so every row's load of the next
+    // step is in flight while this step's FMAs run
+    const int kend = kbeg + kpart;
+    int k0 = kbeg + lane * C;
+    uint4 cur[R];
+    const bool live = n0 < N;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int n = min(n0 + r, N - 1);   // rows past N repeat the last row; their results are not written
-      uint32_t w[C * BITS / 32];
-      load_codes<BITS>(wp + (size_t)n * W + (size_t)k0 * BITS / 32, w);
-      const float s = half_bits_to_float_rt(__ldg(ws + (size_t)n * NG + g), f16 != 0);
-      const float b = half_bits_to_float_rt(__ldg(wb + (size_t)n * NG + g), f16 != 0);
-      float c[C];
-      codes_to_float<BITS>(w, c);
+      cur[r] = live ? __ldcs(reinterpret_cast<const uint4*>(wp + (size_t)n * W + (size_t)k0 * BITS / 32))
+                    : make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (; live && k0 < kend; k0 += 32 * C) {
+      const int kn = k0 + 32 * C;
+      uint4 nxt[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int n = min(n0 + r, N - 1);
+        nxt[r] = kn < kend ? __ldcs(reinterpret_cast<const uint4*>(wp + (size_t)n * W + (size_t)kn * BITS / 32))
+                           : make_uint4(0u, 0u, 0u, 0u);
+      }
+      // the x slice of these C elements, and its sums
+      float2 xv[T][C / 2];
+      float xs[T];
 #pragma unroll
       for (int t = 0; t < T; ++t) {
-        float2 d = make_float2(0.f, 0.f);
+        const uint4* xp = reinterpret_cast<const uint4*>(x + (size_t)t * K + k0);
+        float sum = 0.f;
 #pragma unroll
-        for (int i = 0; i < C / 2; ++i) d = __ffma2_rn(make_float2(c[2 * i], c[2 * i + 1]), xv[t][i], d);
-        acc[r][t] = __ffma2_rn(make_float2(s, s), d, acc[r][t]);
-        bacc[r][t] = fmaf(b, xs[t], bacc[r][t]);
+        for (int q = 0; q < C / 8; ++q) {
+          const uint4 a = __ldg(xp + q);
+          const uint32_t u[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            xv[t][4 * q + i] = make_float2(half_bits_to_float_rt(u[i] & 0xFFFFu, f16 != 0),
+                                           half_bits_to_float_rt(u[i] >> 16, f16 != 0));
+            sum += xv[t][4 * q + i].x + xv[t][4 * q + i].y;
+          }
+        }
+        xs[t] = sum;
+      }
+      const int g = k0 / GS;   // a lane's C elements lie in one group (C <= GS)
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int n = min(n0 + r, N - 1);
+        const float s = half_bits_to_float_rt(__ldg(ws + (size_t)n * NG + g), f16 != 0);
+        const float b = half_bits_to_float_rt(__ldg(wb + (size_t)n * NG + g), f16 != 0);
+        float c[C];
+        codes_to_float<BITS>(cur[r], c);
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          float2 d = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int i = 0; i < C / 2; ++i) d = __ffma2_rn(make_float2(c[2 * i], c[2 * i + 1]), xv[t][i], d);
+          acc[r][t] = __ffma2_rn(make_float2(s, s), d, acc[r][t]);
+          bacc[r][t] = fmaf(b, xs[t], bacc[r][t]);
+        }
+        cur[r] = nxt[r];
       }
     }
-  }
 #pragma unroll
-  for (int r = 0; r < R; ++r)
+    for (int r = 0; r < R; ++r)
 #pragma unroll
-    for (int t = 0; t < T; ++t) {
-      float v = acc[r][t].x + acc[r][t].y + bacc[r][t];
+      for (int t = 0; t < T; ++t) {
+        float v = acc[r][t].x + acc[r][t].y + bacc[r][t];
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane == 0 && n0 + r < N) store_out<OUT>(y, (size_t)t * N + n0 + r, v);
+        for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (S == 1) {   // one part: the warp writes its rows itself
+          if (lane == 0 && n0 + r < N) store_out<OUT>(y, (size_t)t * N + n0 + r, v);
+        } else if (lane == 0) {
+          part[warp][r][t] = v;
+        }
+      }
+    if (S > 1) {
+      __syncthreads();
+      if (sp == 0 && lane < R * T) {   // the S parts of this row group, added in order
+        const int r = lane / T, t = lane - r * T;
+        float v = 0.f;
+        for (int q = 0; q < S; ++q) v += part[warp + q][r][t];
+        if (n0 + r < N) store_out<OUT>(y, (size_t)t * N + n0 + r, v);
+      }
+      __syncthreads();   // the partials are read before the next block of rows overwrites them
     }
+  }
 }
 
 template <int BITS, int T>
 cudaError_t launch_qgemv_t(const uint16_t* x, const uint32_t* wp, const uint16_t* ws, const uint16_t* wb, void* y,
-                           int N, int K, int GS, int f16, int out, cudaStream_t s) {
-  const int rows_per_cta = (kGemvThreads / 32) * kGemvRows;
-  const dim3 grid((unsigned)((N + rows_per_cta - 1) / rows_per_cta));
-  switch (out) {
-    case QDA_BF16: qda_qgemv_kernel<BITS, T, QDA_BF16><<<grid, kGemvThreads, 0, s>>>(x, wp, ws, wb, y, N, K, GS, f16); break;
-    case QDA_FP16: qda_qgemv_kernel<BITS, T, QDA_FP16><<<grid, kGemvThreads, 0, s>>>(x, wp, ws, wb, y, N, K, GS, f16); break;
-    default: qda_qgemv_kernel<BITS, T, QDA_FP32><<<grid, kGemvThreads, 0, s>>>(x, wp, ws, wb, y, N, K, GS, f16); break;
+                           int N, int K, int GS, int f16, int out, int sms, cudaStream_t s) {
+  // K parts per row group: the fewest that give every SM four blocks of rows, as K allows (whole 32-lane steps)
+  int S = 1;
+  while (S < 4 && (long long)(N + (kGemvWarps / S) * kGemvRows - 1) / ((kGemvWarps / S) * kGemvRows) < 4LL * sms &&
+         K % (32 * gemv_codes<BITS>() * S * 2) == 0)
+    S *= 2;
+  const int rows_per_cta = (kGemvWarps / S) * kGemvRows;
+  const long long blocks = (N + rows_per_cta - 1) / rows_per_cta;
+  auto kern = out == QDA_BF16 ? qda_qgemv_kernel<BITS, T, QDA_BF16>
+            : out == QDA_FP16 ? qda_qgemv_kernel<BITS, T, QDA_FP16> : qda_qgemv_kernel<BITS, T, QDA_FP32>;
+  static int occ[3] = {0, 0, 0};   // resident CTAs per SM of each output instance (same on every GB300)
+  int& o = occ[out == QDA_BF16 ? 0 : out == QDA_FP16 ? 1 : 2];
+  if (o == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kGemvThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (o < 1) o = 1;
   }
+  const dim3 grid((unsigned)std::min<long long>(blocks, (long long)sms * o));
+  kern<<<grid, kGemvThreads, 0, s>>>(x, wp, ws, wb, y, N, K, GS, f16, S);
   return cudaGetLastError();
 }
 
 template <int BITS>
 cudaError_t launch_qgemv(const uint16_t* x, const uint32_t* wp, const uint16_t* ws, const uint16_t* wb, void* y,
-                         int T, int N, int K, int GS, int f16, int out, cudaStream_t s) {
+                         int T, int N, int K, int GS, int f16, int out, int sms, cudaStream_t s) {
   switch (T) {
-    case 1: return launch_qgemv_t<BITS, 1>(x, wp, ws, wb, y, N, K, GS, f16, out, s);
-    case 2: return launch_qgemv_t<BITS, 2>(x, wp, ws, wb, y, N, K, GS, f16, out, s);
-    case 3: return launch_qgemv_t<BITS, 3>(x, wp, ws, wb, y, N, K, GS, f16, out, s);
-    default: return launch_qgemv_t<BITS, 4>(x, wp, ws, wb, y, N, K, GS, f16, out, s);
+    case 1: return launch_qgemv_t<BITS, 1>(x, wp, ws, wb, y, N, K, GS, f16, out, sms, s);
+    case 2: return launch_qgemv_t<BITS, 2>(x, wp, ws, wb, y, N, K, GS, f16, out, sms, s);
+    case 3: return launch_qgemv_t<BITS, 3>(x, wp, ws, wb, y, N, K, GS, f16, out, sms, s);
+    default: return launch_qgemv_t<BITS, 4>(x, wp, ws, wb, y, N, K, GS, f16, out, sms, s);
   }
 }
 
@@ -167,7 +215,7 @@ extern "C" int qdecode_qgemv(const void* x, const uint32_t* w_packed, const void
   const int out_dt = out_byte == 0 ? in_dt : out_byte;
   if (bits != 4 && bits != 8) return QDA_ERR_UNSUPPORTED;
   if (GS != 32 && GS != 64 && GS != 128) return QDA_ERR_UNSUPPORTED;
-  if (T > QDA_QGEMV_MAX_T || K % 512 != 0) return QDA_ERR_UNSUPPORTED;
+  if (T > QDA_QGEMV_MAX_T || K % (32 * 128 / bits) != 0) return QDA_ERR_UNSUPPORTED;   // whole 32-lane steps
   const void* ptrs[5] = {x, w_packed, w_scales, w_biases, y};
   for (const void* p : ptrs)
     if (reinterpret_cast<uintptr_t>(p) & 15u) return QDA_ERR_ALIGN;
@@ -176,8 +224,12 @@ extern "C" int qdecode_qgemv(const void* x, const uint32_t* w_packed, const void
   const uint16_t* ws = static_cast<const uint16_t*>(w_scales);
   const uint16_t* wb = static_cast<const uint16_t*>(w_biases);
   const int f16 = in_dt == QDA_FP16;
-  const cudaError_t e = bits == 8 ? qda::launch_qgemv<8>(xs, w_packed, ws, wb, y, T, N, K, GS, f16, out_dt, s)
-                                  : qda::launch_qgemv<4>(xs, w_packed, ws, wb, y, T, N, K, GS, f16, out_dt, s);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return qda_cuda_fail(e);
+  e = bits == 8 ? qda::launch_qgemv<8>(xs, w_packed, ws, wb, y, T, N, K, GS, f16, out_dt, sms, s)
+                : qda::launch_qgemv<4>(xs, w_packed, ws, wb, y, T, N, K, GS, f16, out_dt, sms, s);
   if (e != cudaSuccess) return qda_cuda_fail(e);
   return QDA_OK;
 }

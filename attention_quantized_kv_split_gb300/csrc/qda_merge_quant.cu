@@ -1,4 +1,6 @@
-// Merge kernel (fixed-order combine of the split partials) and the cache quantizer, sm_103a.
+// Merge kernel (fixed-order combine of the split partials), the cache quantizer and the cache-append copy, sm_103a.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -217,36 +219,51 @@ __global__ void __launch_bounds__(256) qda_quant_kernel(const float* __restrict_
   }
 }
 
-// One warp per old row: its K and V words, scales and biases move to the row's place in the appended cache
-// (every KV head's block grows by T rows, so rows shift by the new rows of the blocks before them).
+// The appended cache's row of old row r (every KV head's block grows by T rows, so rows shift by the new rows of
+// the blocks before them).
+__device__ __forceinline__ long long appended_row(const QdaRowMap& m, long long r) {
+  int lo = 0, hi = m.B - 1;   // the last sequence whose old rows start at or before r (skips empty ones)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)m.Hkv * m.off_old[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  const long long local = r - (long long)m.Hkv * m.off_old[lo];
+  const int kvh = (int)(local / m.n_old[lo]);
+  const long long j = local - (long long)kvh * m.n_old[lo];
+  return (long long)m.Hkv * m.off_new[lo] + (long long)kvh * (m.n_old[lo] + m.T) + j;
+}
+
+// Copies the old rows into the appended cache: the K and V codes in 16-byte pieces (a row of W words is W / 4 of
+// them), then each row's scales and biases; grid-stride over both, streaming loads and stores.
 __global__ void __launch_bounds__(256) qda_append_copy_kernel(
     const uint32_t* __restrict__ kp, const uint16_t* __restrict__ ks, const uint16_t* __restrict__ kb,
     const uint32_t* __restrict__ vp, const uint16_t* __restrict__ vs, const uint16_t* __restrict__ vb,
     uint32_t* __restrict__ kpo, uint16_t* __restrict__ kso, uint16_t* __restrict__ kbo, uint32_t* __restrict__ vpo,
     uint16_t* __restrict__ vso, uint16_t* __restrict__ vbo, long long rows_old, int W, int NG,
     const __grid_constant__ QdaRowMap m) {
-  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= rows_old) return;
-  const int lane = threadIdx.x & 31;
-  int lo = 0, hi = m.B - 1;   // the last sequence whose old rows start at or before this row (skips empty ones)
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if ((long long)m.Hkv * m.off_old[mid] <= row) lo = mid; else hi = mid - 1;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int cpr = W / 4;
+  const long long pieces = rows_old * cpr;
+  const uint4* k4 = reinterpret_cast<const uint4*>(kp);
+  const uint4* v4 = reinterpret_cast<const uint4*>(vp);
+  uint4* ko4 = reinterpret_cast<uint4*>(kpo);
+  uint4* vo4 = reinterpret_cast<uint4*>(vpo);
+  for (long long i = tid; i < pieces; i += stride) {
+    const long long r = i / cpr;
+    const long long c = i - r * cpr;
+    const long long d = appended_row(m, r) * cpr + c;
+    __stcs(ko4 + d, __ldcs(k4 + i));
+    __stcs(vo4 + d, __ldcs(v4 + i));
   }
-  const int b = lo;
-  const long long local = row - (long long)m.Hkv * m.off_old[b];
-  const int kvh = (int)(local / m.n_old[b]);
-  const long long j = local - (long long)kvh * m.n_old[b];
-  const long long dst = (long long)m.Hkv * m.off_new[b] + (long long)kvh * (m.n_old[b] + m.T) + j;
-  for (int w = lane; w < W; w += 32) {
-    kpo[dst * W + w] = kp[row * W + w];
-    vpo[dst * W + w] = vp[row * W + w];
-  }
-  for (int g = lane; g < NG; g += 32) {
-    kso[dst * NG + g] = ks[row * NG + g];
-    kbo[dst * NG + g] = kb[row * NG + g];
-    vso[dst * NG + g] = vs[row * NG + g];
-    vbo[dst * NG + g] = vb[row * NG + g];
+  for (long long r = tid; r < rows_old; r += stride) {
+    const long long d = appended_row(m, r) * NG, o = r * NG;
+    for (int g = 0; g < NG; ++g) {
+      kso[d + g] = ks[o + g];
+      kbo[d + g] = kb[o + g];
+      vso[d + g] = vs[o + g];
+      vbo[d + g] = vb[o + g];
+    }
   }
 }
 
@@ -304,7 +321,8 @@ cudaError_t qda_launch_append_copy(const uint32_t* kp, const uint16_t* ks, const
                                    uint16_t* kbo, uint32_t* vpo, uint16_t* vso, uint16_t* vbo, long long rows_old,
                                    int W, int NG, const QdaRowMap& map, cudaStream_t s) {
   if (rows_old <= 0) return cudaSuccess;
-  const unsigned blocks = (unsigned)((rows_old + 7) / 8);
+  const long long pieces = rows_old * (W / 4);
+  const unsigned blocks = (unsigned)std::min<long long>((pieces + 255) / 256, 152LL * 16);
   qda::qda_append_copy_kernel<<<blocks, 256, 0, s>>>(kp, ks, kb, vp, vs, vb, kpo, kso, kbo, vpo, vso, vbo, rows_old,
                                                      W, NG, map);
   return cudaGetLastError();

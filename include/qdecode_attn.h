@@ -202,7 +202,8 @@ int qdecode_quantize(const float* x, long long rows, int D, int GS, int bits, in
  * x [T, K] and the scales and biases in the input dtype of `dtype` (bf16 or fp16); packed [N, K * bits / 32] uint32,
  * codes least-significant first; scales, biases [N, K / GS]; y [T, N] in the output dtype (as for qdecode_attn:
  * 0 = the input dtype). Asynchronous on `stream`, no workspace. Requires bits in {4, 8}, GS in {32, 64, 128},
- * 1 <= T <= QDA_QGEMV_MAX_T and K a multiple of 512 (else QDA_ERR_UNSUPPORTED); pointers 16-byte aligned.
+ * 1 <= T <= QDA_QGEMV_MAX_T and K a multiple of 512 (8-bit) or 1024 (4-bit) (else QDA_ERR_UNSUPPORTED); pointers
+ * 16-byte aligned.
  */
 #define QDA_QGEMV_MAX_T 4
 int qdecode_qgemv(const void* x, const uint32_t* w_packed, const void* w_scales, const void* w_biases, void* y,

@@ -58,6 +58,14 @@ def test_qgemv_sweep(bits, GS, T):
 @pytest.mark.parametrize("N", [1, 3, 31, 32, 33, 1000])
 def test_qgemv_row_counts(N):
     check(2, N, 512, 64, 8, seed=N)
+    check(1, N, 1024, 32, 4, seed=N + 1)
+
+
+@pytest.mark.parametrize("K,N", [(14336, 4096), (8192, 512), (3072, 7)])
+def test_qgemv_k_split(K, N):
+    # few row groups: K is split across warps (2 or 4 parts) to fill the GPU
+    check(1, N, K, 64, 8, seed=K + N)
+    check(3, N, K, 128, 4, out="bf16", seed=K + N + 1)
 
 
 @pytest.mark.parametrize("dtype,out", [("bf16", "bf16"), ("fp16", "fp16"), ("fp16", "fp32"), ("bf16", "fp16")])
