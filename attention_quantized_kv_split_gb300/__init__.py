@@ -146,6 +146,11 @@ def qdecode_attn_debug_force_splits(num_ctas: int) -> None:
     _lib.check(lib().qdecode_attn_debug_force_splits(num_ctas), "qdecode_attn_debug_force_splits")
 
 
+def qdecode_attn_debug_stall_chunk(chunk: int) -> None:
+    """Testing aid: the first CTA's producer stops before its chunk ``chunk`` (-1: off); see the C header."""
+    _lib.check(lib().qdecode_attn_debug_stall_chunk(chunk), "qdecode_attn_debug_stall_chunk")
+
+
 def qdecode_attn_set_split_event(event: Optional[torch.cuda.Event]) -> None:
     handle = None if event is None else event.cuda_event
     _lib.check(lib().qdecode_attn_set_split_event(handle), "qdecode_attn_set_split_event")

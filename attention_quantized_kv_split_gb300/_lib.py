@@ -55,6 +55,7 @@ SIGNATURES = {
     "qdecode_attn_workspace_bytes": (_I, [_I, _I, _I, _PI32, _I, _I, _I, ctypes.POINTER(_SZ)]),
     "qdecode_attn_set_workspace": (_I, [_P, _SZ]),
     "qdecode_attn_debug_force_splits": (_I, [_I]),
+    "qdecode_attn_debug_stall_chunk": (_I, [_I]),
     "qdecode_attn_set_split_event": (_I, [_P]),
     "qdecode_qgemv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "qdecode_cache_append": (_I, [_P] * 14 + [_I, _I, _PI32, _I, _I, _I, _I, _I, _P]),

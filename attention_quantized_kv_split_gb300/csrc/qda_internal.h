@@ -29,6 +29,7 @@ struct QdaParams {
   int mode;                   // lean split kernel: 0 single-pass, 1 multi-query, 2 compat pass A, 3 compat pass B
   int k_only;                 // the ring carries K only (compat pass A)
   int compat;                 // merge: plain sum of the partials (compat pass B wrote normalised sums)
+  int stall_chunk;            // testing aid: CTA 0's producer stops before this chunk (-1: never)
   int tile_shift;             // log2(tile_rows): pipeline tiles are powers of two
   int f16;                    // q / scales / biases are fp16 (else bf16)
   float qscale;               // log2(e) / sqrt(D): scores come out in log2 units

@@ -19,6 +19,7 @@ constexpr long long kMaxCtas = 4096;   // the merge kernel stages one weight per
 thread_local int t_last_cuda_error = 0;
 thread_local void* t_split_event = nullptr;
 std::atomic<int> g_force_splits{0};
+std::atomic<int> g_stall_chunk{-1};
 std::atomic<long long> g_calls{0};
 
 __device__ unsigned int g_device_err;
@@ -345,6 +346,7 @@ int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, cons
   p.tile_shift = 0;
   while ((1 << p.tile_shift) < v.tile) ++p.tile_shift;
   p.f16 = in_dt == QDA_FP16 ? 1 : 0;
+  p.stall_chunk = g_stall_chunk.load();
   // scores in log2 units, except in the compat form, which rounds them in natural units first
   p.qscale = (compat ? 1.0f : 1.4426950408889634f) / sqrtf((float)D);
   p.seq_off[0] = 0;
@@ -416,6 +418,11 @@ int qdecode_attn_set_workspace(void* ptr, size_t bytes) {
 int qdecode_attn_debug_force_splits(int num_ctas) {
   if (num_ctas < 0) return QDA_ERR_INVALID;
   g_force_splits.store(num_ctas);
+  return QDA_OK;
+}
+
+int qdecode_attn_debug_stall_chunk(int chunk) {
+  g_stall_chunk.store(chunk < 0 ? -1 : chunk);
   return QDA_OK;
 }
 

@@ -272,8 +272,10 @@ def run_ours(args):
     torch.cuda.synchronize()
     t0 = time.time()
     calls_before = qda.qdecode_attn_calls()
+    torch.cuda.nvtx.range_push("timed decode calls")
     ms = time_calls(call, args.steps, flush, stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     if world > 1:
         dist.barrier()
     t1 = time.time()
@@ -332,6 +334,7 @@ def run_ours(args):
     h2d = hq.numel() * hq.element_size() + sum(t.numel() * t.element_size() for t in host)
     d2h = hout.numel() * hout.element_size()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("end-to-end calls (host buffers)")
     e0.record(stream)
     for _ in range(esteps):
         dq.copy_(hq, non_blocking=True)
@@ -341,6 +344,7 @@ def run_ours(args):
         hout.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     e2e_ms = e0.elapsed_time(e1) / esteps
     e2e = {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": esteps}

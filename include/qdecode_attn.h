@@ -177,6 +177,14 @@ int qdecode_attn_set_workspace(void* ptr, size_t bytes);
 int qdecode_attn_debug_force_splits(int num_ctas);
 
 /*
+ * Testing aid for failure detection: with chunk >= 0, the producer of the first CTA of later calls (from every
+ * thread) stops before its chunk number `chunk`, so that CTA's consumers wait for data that never comes. Their
+ * bounded wait gives up after its time limit (about one second), the call's output is invalid and
+ * qdecode_attn_device_status() reports bit 1; the context stays usable. chunk < 0 switches it off.
+ */
+int qdecode_attn_debug_stall_chunk(int chunk);
+
+/*
  * Timing aid: when `event` (a cudaEvent_t) is non-NULL, later qdecode_attn calls from this host thread record it
  * on the stream between the split kernel and the merge kernel (the merge then launches without programmatic
  * dependent launch). NULL switches it off.
