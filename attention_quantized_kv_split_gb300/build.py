@@ -18,6 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqdecode_attn.so")
+# checked build: every index check of the kernels compiled in (a failed check sets bit 4 of the device status)
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "libqdecode_attn_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
@@ -50,16 +53,18 @@ def _compile(src: str, obj: str, extra) -> str:
     return r.stderr
 
 
-def build(verbose: bool = False, ptxas_info: bool = False, jobs: int = 0) -> str:
-    """Compile every .cu under csrc/ and link libqdecode_attn.so; returns the library path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, ptxas_info: bool = False, jobs: int = 0, checked: bool = False) -> str:
+    """Compile every .cu under csrc/ and link libqdecode_attn.so (or, with checked=True, the bounds-checked
+    libqdecode_attn_checked.so); returns the library path."""
+    bdir, lib = (BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD, LIB)
+    os.makedirs(bdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     deps = _deps()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DQDA_BOUNDS_CHECK"] if checked else [])
     todo = []
     objs = []
     for s in srcs:
-        o = os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
+        o = os.path.join(bdir, os.path.basename(s)[:-3] + ".o")
         objs.append(o)
         if ptxas_info or _stale(o, [s, *deps]):
             todo.append((s, o))
@@ -71,14 +76,14 @@ def build(verbose: bool = False, ptxas_info: bool = False, jobs: int = 0) -> str
                 msg = f.result()
                 if verbose and msg:
                     print(f"--- {os.path.basename(futs[f])}\n{msg}", file=sys.stderr)
-    if todo or _stale(LIB, objs):
-        tmp = LIB + ".tmp"
+    if todo or _stale(lib, objs):
+        tmp = lib + ".tmp"
         cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(kMergeThreads) qda_merge_kernel(const __grid_c
 #pragma unroll 4
   for (int k = grp; k < ns; k += groups) {
     const int c = cf + k;
+    if (!in_bounds(c + unit < C + p.B * p.Hkv && j < p.heads_pad, p.err)) continue;
     const size_t hp = (size_t)(c + unit) * p.heads_pad + j;
     const float2 ml = p.part_ml[hp];
     const float4 v = reinterpret_cast<const float4*>(p.part_o + hp * D)[t];

@@ -5,6 +5,17 @@
 
 namespace qda {
 
+// Index checks of a checked build (compiled with QDA_BOUNDS_CHECK): a failed check sets bit 4 of the device error
+// word and the caller skips the access. In the normal build every check is the constant true.
+#ifdef QDA_BOUNDS_CHECK
+__device__ __forceinline__ bool in_bounds(bool ok, unsigned int* err) {
+  if (!ok) atomicOr(err, 4u);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(bool, unsigned int*) { return true; }
+#endif
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

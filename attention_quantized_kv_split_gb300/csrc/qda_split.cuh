@@ -50,6 +50,7 @@ __device__ __forceinline__ void unit_stats(const QdaParams& p, long long T, long
   for (int k = threadIdx.x & 31; k < ns; k += 32) {
     const int c = cf + k;
     if (maybe_empty && qda_cta_row(T, C, c) == qda_cta_row(T, C, c + 1)) continue;
+    if (!in_bounds(c + unit < C + p.B * p.Hkv && head < p.heads_pad, p.err)) continue;
     const float2 ml = p.part_ml[(size_t)(c + unit) * p.heads_pad + head];
     const float mn = fmaxf(M, ml.x);
     den = (M == -INFINITY ? 0.f : den * exp2f(M - mn)) + ml.y * exp2f(ml.x - mn);
@@ -133,6 +134,11 @@ __device__ __forceinline__ void issue_chunk(const QdaParams& p, unsigned char* s
   const uint32_t s16 = sbytes & ~15u;
   const size_t soff = (size_t)(s0 - t0) * SB;
   const int arrays = p.k_only ? 2 : 4;   // scale/bias arrays copied: K's, and V's unless the ring carries K only
+  // the chunk lies in the tile and the arrays; else (checked build) the phase completes with no bytes
+  const bool inb = in_bounds(c0 >= t0 && c0 < c1 && c1 <= T && s1 <= T && coff + cbytes <= L.codes_bytes &&
+                             s0 >= t0 && soff + sbytes <= L.sc_bytes, p.err);
+  if (lane == 0 && !inb) mbar_arrive_expect_tx(&full[s], 0);
+  if (!inb) return;
   if (lane == 0) {
     if (s16 != sbytes) {
       const uint16_t* srcs[4] = {p.ks, p.kb, p.vs, p.vb};
@@ -257,7 +263,8 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
         const int j = hc * NH + h;
         float acc = 0.f;
         hide[h] = qda_hidden_tail(j, p.nrep, p.L);
-        if (j < p.nrep * p.L) {
+        if (j < p.nrep * p.L &&
+            in_bounds(qda_q_row(walk.b, walk.kvh, j, p.nrep, p.L, p.H) < (long long)p.B * p.L * p.H, p.err)) {
           const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
                                qda_q_row(walk.b, walk.kvh, j, p.nrep, p.L, p.H) * D + lir * E;
 #pragma unroll
@@ -295,6 +302,7 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
         const long long row = rb + rir;
         const bool valid = row < c1;
         const int lr = (int)((valid ? row : c0) - t0);
+        if (!in_bounds(lr >= 0 && lr < TILE, p.err)) continue;
         // K: factored dot over this lane's slice, then the sum over the LPR lanes of the row
         float cf[E];
 #pragma unroll
@@ -415,6 +423,7 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
           Ls = fmaf(comb_l[w * NH + h], wt, Ls);
         }
         const size_t hp = (size_t)slot * p.heads_pad + (size_t)hc * NH + h;
+        if (!in_bounds(slot < (long long)p.num_ctas + p.B * p.Hkv && hc * NH + h < p.heads_pad, p.err)) continue;
         if constexpr (!STATS) p.part_o[hp * D + d] = O;
         if (!APPLY && d == 0) p.part_ml[hp] = make_float2(M, Ls);
       }

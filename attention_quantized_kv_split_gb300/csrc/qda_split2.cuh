@@ -252,7 +252,8 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       for (int h = 0; h < NH; ++h) {
         const int j = hc * NH + h;
         float acc = 0.f;
-        if (j < p.nrep * p.L) {
+        if (j < p.nrep * p.L &&
+            in_bounds(qda_q_row(walk.b, walk.kvh, j, p.nrep, p.L, p.H) < (long long)p.B * p.L * p.H, p.err)) {
           const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
                                qda_q_row(walk.b, walk.kvh, j, p.nrep, p.L, p.H) * D + klane * EK;
           const uint4 a = reinterpret_cast<const uint4*>(qp)[0];
@@ -290,6 +291,7 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
         for (int k = lane >> LOG_NH; k < ns; k += 32 >> LOG_NH) {
           const int c = cf + k;
           if (maybe_empty && qda_cta_row(T, C, c) == qda_cta_row(T, C, c + 1)) continue;
+          if (!in_bounds(c + walk.unit < C + p.B * p.Hkv, p.err)) continue;
           const float2 ml = p.part_ml[(size_t)(c + walk.unit) * p.heads_pad + hc * NH + my_h];
           const float mn = fmaxf(M, ml.x);
           den = den * ex2(M - mn) + ml.y * ex2(ml.x - mn);
@@ -314,6 +316,8 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       const int rows_valid = (int)min((long long)R, c1 - b0);
       const unsigned char* st = smem + L.stage0 + (size_t)stage * L.stage_bytes;
       const int lr0 = (int)(b0 - t0);                       // block's first row within the stage
+      // the block's rows [lr0, lr0 + rows_valid) lie in the stage (loads past rows_valid clamp to its last row)
+      if (!in_bounds(lr0 >= 0 && rows_valid > 0 && lr0 + rows_valid <= TILE, p.err)) continue;
       const uint32_t* sK = reinterpret_cast<const uint32_t*>(st) + (size_t)lr0 * W;
       const uint32_t* sV = reinterpret_cast<const uint32_t*>(st + L.codes_bytes) + (size_t)lr0 * W;
       const uint16_t* sKS = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes) + lr0 * NG;
@@ -532,6 +536,7 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
           Ls = fmaf(comb_l[w * NH + h], wt, Ls);
         }
         const size_t hp = (size_t)slot * p.heads_pad + (size_t)hc * NH + h;
+        if (!in_bounds(slot < (long long)p.num_ctas + p.B * p.Hkv && hc * NH + h < p.heads_pad, p.err)) continue;
         if constexpr (!STATS) p.part_o[hp * D + d] = O;
         if (!APPLY && d == 0) p.part_ml[hp] = make_float2(M, Ls);
       }
