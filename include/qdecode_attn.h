@@ -240,7 +240,9 @@ int qdecode_attn_last_cuda_error(void);
 
 /*
  * Device-side status: copies (synchronously) and clears the current device's error word. Bits: 1 = a pipeline
- * wait in the split kernel gave up after its time limit (the output of that call is invalid). 0 = clean.
+ * wait in the split kernel gave up after its time limit (the output of that call is invalid); 2 = waiting for the
+ * CTA's own copies to land before it exits gave up; 4 = an index check failed (only a library built with
+ * QDA_BOUNDS_CHECK checks, and it skips the access). 0 = clean.
  */
 int qdecode_attn_device_status(unsigned int* flags);
 
