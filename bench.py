@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2)
-    ap.add_argument("--no-extra", action="store_true", help="skip the per-workload figures (workloads 3-5, multi-query decode, two-pass compat form, 8-bit GEMV, cache append)")
+    ap.add_argument("--no-extra", action="store_true", help="skip the per-workload figures (workloads 3-5, multi-query, compat, GEMV, cache append, graph replay)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -410,6 +410,23 @@ def run_ours(args):
             "us_per_call": round(ma * 1e3, 2), "GBps": round(abytes / (ma * 1e-3) / 1e9, 1),
             "frac_of_peak": round(abytes / (ma * 1e-3) / 1e9 / peak, 4), "bytes_moved": abytes}
         del akn, avn, anext
+        # this workload's call captured once in a CUDA graph and replayed (split + merge, no host launch work)
+        og = torch.empty_like(out)
+        gs_ = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gs_):
+            with torch.cuda.graph(graph, stream=gs_):
+                qda.qdecode_attn(q, cache.kp, cache.ks, cache.kb, cache.vp, cache.vs, cache.vb, og, N, w.Hkv, w.GS,
+                                 w.bits, gs_)
+        gcall2 = lambda: graph.replay()
+        for _ in range(5):
+            gcall2()
+        torch.cuda.synchronize()
+        mgr = statistics.median(time_calls(gcall2, 50, flush, torch.cuda.current_stream()))
+        extra[f"{w.name}_graph_replay"] = {"us_per_call": round(mgr * 1e3, 2),
+                                           "kv_GBps": round(nbytes / (mgr * 1e-3) / 1e9, 1),
+                                           "frac_of_peak": round(nbytes / (mgr * 1e-3) / 1e9 / peak, 4)}
+        del graph, og
         # small-L multi-query decode on this workload's cache: 4 query positions (the last 4 tokens) per sequence
         Lq = 4
         qm = synth.query_multi(w, Lq).to(device)
