@@ -8,9 +8,9 @@
 // over every SM); each step a lane takes 128 bits of codes (16 elements of 8-bit, 32 of 4-bit) per row, streamed
 // past L1, the x slice of those elements (read through the read-only path: every warp reads the same few KB of x),
 // and the row's scale and bias of that group. The dot is factored as in the attention kernels: s * sum(x * code) +
-// b * sum(x), with exact codes (2^23 + code minus 2^23) and packed f32x2 FMAs. Lanes reduce by shuffles, the S
-// parts meet in shared memory in a fixed order, and one lane writes the rounded outputs. The weights are streamed
-// once: a matrix-vector product is bound by HBM.
+// b * sum(x), with exact codes (a byte permute to 2^23 + code, minus 2^23) and packed f32x2 FMAs. Lanes reduce
+// by shuffles, the S parts meet in shared memory in a fixed order, and one lane writes the rounded outputs. The
+// weights are streamed once: a matrix-vector product is bound by HBM.
 #include <algorithm>
 
 #include <cuda_bf16.h>
@@ -29,17 +29,24 @@ constexpr int kGemvWarps = kGemvThreads / 32;
 template <int BITS>
 __host__ __device__ constexpr int gemv_codes() { return 128 / BITS; }
 
-// codes of one 128-bit load as exact floats, in element order
+// The codes of one word as exact float pairs (code 2j, code 2j + 1): a byte permute puts each code under the
+// exponent byte of 2^23 ([code, 0, 0, 0x4B] = 2^23 + code) and one packed subtract removes 2^23.
 template <int BITS>
-__device__ __forceinline__ void codes_to_float(const uint4 v, float (&c)[128 / BITS]) {
-  constexpr int PER = 32 / BITS;
-  constexpr uint32_t MASK = (1u << BITS) - 1u;
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+__device__ __forceinline__ void word_to_float(uint32_t w, float2 (&c)[16 / BITS]) {
+  const float2 off = make_float2(-8388608.0f, -8388608.0f);
+  if constexpr (BITS == 8) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+    for (int j = 0; j < 2; ++j)
+      c[j] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7650u | (2 * j))),
+                                    __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7651u | (2 * j)))), off);
+  } else {
+    const uint32_t lo = w & 0x0F0F0F0Fu;          // codes 0, 2, 4, 6 of the word in bytes 0..3
+    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;   // codes 1, 3, 5, 7
 #pragma unroll
-    for (int k = 0; k < PER; ++k)
-      c[i * PER + k] = __uint_as_float(0x4B000000u | ((w[i] >> (BITS * k)) & MASK)) - 8388608.0f;
+    for (int j = 0; j < 4; ++j)
+      c[j] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7650u | j)),
+                                    __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7650u | j))), off);
+  }
 }
 
 template <int OUT>
@@ -53,9 +60,11 @@ __device__ __forceinline__ void store_out(void* y, size_t idx, float v) {
   }
 }
 
-// resident CTAs per SM the register budget aims at: three for one input row, fewer as the accumulators grow
+// resident CTAs per SM the register budget aims at: three for one input row of 8-bit codes, fewer as the x slice
+// (4-bit codes: 32 elements a step) and the accumulators grow
 template <int BITS, int T, int OUT>
-__global__ void __launch_bounds__(kGemvThreads, T == 1 ? 3 : T == 2 ? 2 : 1) qda_qgemv_kernel(const uint16_t* __restrict__ x,
+__global__ void __launch_bounds__(kGemvThreads, T == 1 ? (BITS == 8 ? 3 : 2) : (T == 2 && BITS == 8) ? 2 : 1)
+    qda_qgemv_kernel(const uint16_t* __restrict__ x,
                                                                 const uint32_t* __restrict__ wp,
                                                                 const uint16_t* __restrict__ ws,
                                                                 const uint16_t* __restrict__ wb, void* __restrict__ y,
@@ -129,14 +138,24 @@ __global__ void __launch_bounds__(kGemvThreads, T == 1 ? 3 : T == 2 ? 2 : 1) qda
         const int n = min(n0 + r, N - 1);
         const float s = half_bits_to_float_rt(__ldg(ws + (size_t)n * NG + g), f16 != 0);
         const float b = half_bits_to_float_rt(__ldg(wb + (size_t)n * NG + g), f16 != 0);
-        float c[C];
-        codes_to_float<BITS>(cur[r], c);
+        // one word of codes at a time: only its pairs are live
+        constexpr int PW = 16 / BITS;   // code pairs per word
+        const uint32_t wv[4] = {cur[r].x, cur[r].y, cur[r].z, cur[r].w};
+        float2 d[T];
+#pragma unroll
+        for (int t = 0; t < T; ++t) d[t] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float2 c[PW];
+          word_to_float<BITS>(wv[i], c);
+#pragma unroll
+          for (int t = 0; t < T; ++t)
+#pragma unroll
+            for (int j = 0; j < PW; ++j) d[t] = __ffma2_rn(c[j], xv[t][PW * i + j], d[t]);
+        }
 #pragma unroll
         for (int t = 0; t < T; ++t) {
-          float2 d = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int i = 0; i < C / 2; ++i) d = __ffma2_rn(make_float2(c[2 * i], c[2 * i + 1]), xv[t][i], d);
-          acc[r][t] = __ffma2_rn(make_float2(s, s), d, acc[r][t]);
+          acc[r][t] = __ffma2_rn(make_float2(s, s), d[t], acc[r][t]);
           bacc[r][t] = fmaf(b, xs[t], bacc[r][t]);
         }
         cur[r] = nxt[r];

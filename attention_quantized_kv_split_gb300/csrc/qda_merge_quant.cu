@@ -220,50 +220,42 @@ __global__ void __launch_bounds__(256) qda_quant_kernel(const float* __restrict_
   }
 }
 
-// The appended cache's row of old row r (every KV head's block grows by T rows, so rows shift by the new rows of
-// the blocks before them).
-__device__ __forceinline__ long long appended_row(const QdaRowMap& m, long long r) {
-  int lo = 0, hi = m.B - 1;   // the last sequence whose old rows start at or before r (skips empty ones)
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if ((long long)m.Hkv * m.off_old[mid] <= r) lo = mid; else hi = mid - 1;
-  }
-  const long long local = r - (long long)m.Hkv * m.off_old[lo];
-  const int kvh = (int)(local / m.n_old[lo]);
-  const long long j = local - (long long)kvh * m.n_old[lo];
-  return (long long)m.Hkv * m.off_new[lo] + (long long)kvh * (m.n_old[lo] + m.T) + j;
-}
+// Copies the old rows of the (sequence, KV head) units into the appended cache: CTA (x, y) takes rows
+// [x * kAppendRows, (x + 1) * kAppendRows) of units y, y + gridDim.y, ... A unit's old rows are contiguous in both caches (its block
+// only moves by the new rows of the blocks before it), so the K and V codes go as flat 16-byte pieces and the
+// scales and biases as flat 16-bit values; streaming loads and stores.
+constexpr int kAppendRows = 128;
 
-// Copies the old rows into the appended cache: the K and V codes in 16-byte pieces (a row of W words is W / 4 of
-// them), then each row's scales and biases; grid-stride over both, streaming loads and stores.
 __global__ void __launch_bounds__(256) qda_append_copy_kernel(
     const uint32_t* __restrict__ kp, const uint16_t* __restrict__ ks, const uint16_t* __restrict__ kb,
     const uint32_t* __restrict__ vp, const uint16_t* __restrict__ vs, const uint16_t* __restrict__ vb,
     uint32_t* __restrict__ kpo, uint16_t* __restrict__ kso, uint16_t* __restrict__ kbo, uint32_t* __restrict__ vpo,
-    uint16_t* __restrict__ vso, uint16_t* __restrict__ vbo, long long rows_old, int W, int NG,
-    const __grid_constant__ QdaRowMap m) {
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const int cpr = W / 4;
-  const long long pieces = rows_old * cpr;
-  const uint4* k4 = reinterpret_cast<const uint4*>(kp);
-  const uint4* v4 = reinterpret_cast<const uint4*>(vp);
-  uint4* ko4 = reinterpret_cast<uint4*>(kpo);
-  uint4* vo4 = reinterpret_cast<uint4*>(vpo);
-  for (long long i = tid; i < pieces; i += stride) {
-    const long long r = i / cpr;
-    const long long c = i - r * cpr;
-    const long long d = appended_row(m, r) * cpr + c;
-    __stcs(ko4 + d, __ldcs(k4 + i));
-    __stcs(vo4 + d, __ldcs(v4 + i));
-  }
-  for (long long r = tid; r < rows_old; r += stride) {
-    const long long d = appended_row(m, r) * NG, o = r * NG;
-    for (int g = 0; g < NG; ++g) {
-      kso[d + g] = ks[o + g];
-      kbo[d + g] = kb[o + g];
-      vso[d + g] = vs[o + g];
-      vbo[d + g] = vb[o + g];
+    uint16_t* __restrict__ vso, uint16_t* __restrict__ vbo, int W, int NG, const __grid_constant__ QdaRowMap m) {
+  for (int unit = blockIdx.y; unit < m.B * m.Hkv; unit += gridDim.y) {
+    const int b = unit / m.Hkv, kvh = unit - b * m.Hkv;
+    const long long n = m.n_old[b];
+    const long long r0 = (long long)blockIdx.x * kAppendRows;
+    if (r0 >= n) continue;
+    const long long rows = min((long long)kAppendRows, n - r0);
+    const long long src = (long long)m.Hkv * m.off_old[b] + kvh * n + r0;              // first row, old cache
+    const long long dst = (long long)m.Hkv * m.off_new[b] + kvh * (n + m.T) + r0;      // its row, new cache
+    const int cpr = W / 4;   // 16-byte pieces per row
+    const uint4* k4 = reinterpret_cast<const uint4*>(kp) + src * cpr;
+    const uint4* v4 = reinterpret_cast<const uint4*>(vp) + src * cpr;
+    uint4* ko4 = reinterpret_cast<uint4*>(kpo) + dst * cpr;
+    uint4* vo4 = reinterpret_cast<uint4*>(vpo) + dst * cpr;
+    const long long pieces = rows * cpr;
+    for (long long i = threadIdx.x; i < pieces; i += blockDim.x) {
+      const uint4 a = __ldcs(k4 + i), c = __ldcs(v4 + i);
+      __stcs(ko4 + i, a);
+      __stcs(vo4 + i, c);
+    }
+    const long long e = rows * NG;
+    for (long long i = threadIdx.x; i < e; i += blockDim.x) {
+      kso[dst * NG + i] = ks[src * NG + i];
+      kbo[dst * NG + i] = kb[src * NG + i];
+      vso[dst * NG + i] = vs[src * NG + i];
+      vbo[dst * NG + i] = vb[src * NG + i];
     }
   }
 }
@@ -322,9 +314,10 @@ cudaError_t qda_launch_append_copy(const uint32_t* kp, const uint16_t* ks, const
                                    uint16_t* kbo, uint32_t* vpo, uint16_t* vso, uint16_t* vbo, long long rows_old,
                                    int W, int NG, const QdaRowMap& map, cudaStream_t s) {
   if (rows_old <= 0) return cudaSuccess;
-  const long long pieces = rows_old * (W / 4);
-  const unsigned blocks = (unsigned)std::min<long long>((pieces + 255) / 256, 152LL * 16);
-  qda::qda_append_copy_kernel<<<blocks, 256, 0, s>>>(kp, ks, kb, vp, vs, vb, kpo, kso, kbo, vpo, vso, vbo, rows_old,
-                                                     W, NG, map);
+  int max_n = 0;
+  for (int b = 0; b < map.B; ++b) max_n = std::max(max_n, map.n_old[b]);
+  const dim3 grid((unsigned)((max_n + qda::kAppendRows - 1) / qda::kAppendRows),
+                  (unsigned)std::min(map.B * map.Hkv, 65535));
+  qda::qda_append_copy_kernel<<<grid, 256, 0, s>>>(kp, ks, kb, vp, vs, vb, kpo, kso, kbo, vpo, vso, vbo, W, NG, map);
   return cudaGetLastError();
 }
