@@ -18,6 +18,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "qda_split.cuh"
 
 namespace qda {
@@ -311,19 +313,20 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
     }
 
     const bool ok = mbar_wait_bounded(&full[stage], phase, abort_flag, p.err, 1u);
-    // the chunk's rows are dealt to the warps in blocks of R
-    for (long long b0 = c0 + (long long)warp * R; ok && b0 < c1; b0 += (long long)NW * R) {
-      const int rows_valid = (int)min((long long)R, c1 - b0);
+    // one block of R rows of the chunk (FULL) or its last, shorter block: a full block's row indexes are constants
+    auto block = [&](auto full_tag, const long long b0, const int rows_in) {
+      constexpr bool FULL = decltype(full_tag)::value;
+      const int rows_valid = FULL ? R : rows_in;
       const unsigned char* st = smem + L.stage0 + (size_t)stage * L.stage_bytes;
       const int lr0 = (int)(b0 - t0);                       // block's first row within the stage
       // the block's rows [lr0, lr0 + rows_valid) lie in the stage (loads past rows_valid clamp to its last row)
-      if (!in_bounds(lr0 >= 0 && rows_valid > 0 && lr0 + rows_valid <= TILE, p.err)) continue;
+      if (!in_bounds(lr0 >= 0 && rows_valid > 0 && lr0 + rows_valid <= TILE, p.err)) return;
       const uint32_t* sK = reinterpret_cast<const uint32_t*>(st) + (size_t)lr0 * W;
       const uint32_t* sV = reinterpret_cast<const uint32_t*>(st + L.codes_bytes) + (size_t)lr0 * W;
       const uint16_t* sKS = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes) + lr0 * NG;
       const uint16_t* sKB = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes + L.sc_bytes) + lr0 * NG;
-      const uint16_t* sVS = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes + 2 * L.sc_bytes) + lr0 * NG;
-      const uint16_t* sVB = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes + 3 * L.sc_bytes) + lr0 * NG;
+      [[maybe_unused]] const uint16_t* sVS = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes + 2 * L.sc_bytes) + lr0 * NG;
+      [[maybe_unused]] const uint16_t* sVB = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes + 3 * L.sc_bytes) + lr0 * NG;
 
       // ---- phase 0: per-(row, group) coefficients of K and V (a fixed trip count, so all the loads issue at once)
       constexpr int P0 = (R * NG + 31) / 32;
@@ -391,13 +394,15 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       }
       float sc[NVL];
       int rr[NVL];
+      bool vis[NVL];   // row rr[i] is in the block and visible to my head (always, in a full single-position block)
       float bm = -INFINITY;
 #pragma unroll
       for (int i = 0; i < NVL; ++i) {
         rr[i] = my_s[i] * RPS + khalf;
         float si = v[i];
         if constexpr (COMPAT) si = round_to_input(si, f16) * LOG2E;   // natural units, rounded, then log2 units
-        sc[i] = rr[i] < seen ? si : -INFINITY;
+        vis[i] = (FULL && !MULTI) || rr[i] < seen;
+        sc[i] = vis[i] ? si : -INFINITY;
         bm = fmaxf(bm, sc[i]);
       }
       // lazy rescaling: the reference max m_run of a head moves only when one of its scores exceeds it by more than
@@ -426,10 +431,10 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       for (int i = 0; i < NVL; ++i) {
         float2* ps = reinterpret_cast<float2*>(sPS) + 2 * (rr[i] * PS_ROW + (my_h >> 1) * NG) + (my_h & 1);
         if constexpr (STATS) {
-          if (rr[i] < seen) psum += ex2(sc[i] - m_run);
+          if (vis[i]) psum += ex2(sc[i] - m_run);
           continue;
         }
-        if (rr[i] < seen) {
+        if (vis[i]) {
           float pr = ex2(sc[i] - m_run);
           if constexpr (APPLY) pr = round_to_input(pr * inv_den, f16);   // normalised, rounded to the input dtype
           psum += pr;
@@ -450,7 +455,7 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       __syncwarp();
 
       // ---- phase 4: V accumulation (none in pass A)
-      if constexpr (STATS) continue;
+      if constexpr (STATS) return;
       if (moved) {
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
@@ -478,6 +483,17 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
         }
       }
       __syncwarp();
+    };
+    // the chunk's rows are dealt to the warps in blocks of R
+    for (long long b0 = c0 + (long long)warp * R; ok && b0 < c1; b0 += (long long)NW * R) {
+      const int rows = (int)min((long long)R, c1 - b0);
+      // the full-block copy pays with 4 heads per CTA (shorter blocks, more of the work in row indexing); with 2 the
+      // larger code is slower
+      if (NH == 4 && rows == R) {
+        block(std::true_type{}, b0, rows);
+      } else {
+        block(std::false_type{}, b0, rows);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
