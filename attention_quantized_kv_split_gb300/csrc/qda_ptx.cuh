@@ -3,6 +3,8 @@
 
 #include <cstdint>
 
+#include <cuda_fp16.h>
+
 namespace qda {
 
 // Index checks of a checked build (compiled with QDA_BOUNDS_CHECK): a failed check sets bit 4 of the device error
@@ -134,6 +136,12 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t u16) {
 // bf16 or fp16 bits -> float, dtype chosen at run time (a warp-uniform select)
 __device__ __forceinline__ float half_bits_to_float_rt(uint32_t u16, bool f16) {
   return f16 ? fp16_bits_to_float(u16) : bf16_bits_to_float(u16);
+}
+
+// Two bf16 or fp16 values packed in a word (first in the low half) -> float2, dtype chosen at run time.
+__device__ __forceinline__ float2 half2_bits_to_float2_rt(uint32_t w, bool f16) {
+  if (f16) return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
 }  // namespace qda

@@ -176,6 +176,13 @@ __device__ __forceinline__ void produce_range(const QdaParams& p, ChunkWalker wa
   int s = 0, ph = 0;   // ring slot of chunk i and the parity of its use (i / STAGES) & 1
   while (walk.next(p, c0, c1, t0)) {
     if (blockIdx.x == 0 && i == p.stall_chunk) break;   // testing aid: the consumers' wait for it must run out
+    if (i == 1) {
+      // the second chunk goes out once the first has landed: every CTA's first chunk then comes in one short burst
+      // ahead of the rest, so the consumers start sooner (the ring still fills while they work on it)
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(&full[0], 0, abort_flag, p.err, 1u);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    }
     if (i >= STAGES) {
       int ok = 1;
       if (lane == 0) ok = mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, p.err, 1u);

@@ -101,6 +101,22 @@ __device__ __forceinline__ float2 coeffs(float s, float b) {
   }
 }
 
+// The same for two groups at once: (s, b) pairs -> A in .x, B in .y of the
+// results' pairs (A pair, B pair).
+template <int BITS, bool EXACT>
+__device__ __forceinline__ void coeffs2(float2 s, float2 b, float2& A, float2& B) {
+  if constexpr (EXACT) {
+    A = s;
+    B = b;
+  } else if constexpr (BITS == 4) {
+    A = __fmul2_rn(make_float2(256.0f, 256.0f), s);
+    B = __ffma2_rn(make_float2(-128.0f, -128.0f), s, b);
+  } else {
+    A = __fmul2_rn(make_float2(32768.0f, 32768.0f), s);
+    B = __ffma2_rn(make_float2(-32768.0f, -32768.0f), s, b);
+  }
+}
+
 template <int N>
 __device__ __forceinline__ void load_words(const uint32_t* src, uint32_t (&w)[N]) {
   if constexpr (N == 1) {
@@ -328,10 +344,13 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       [[maybe_unused]] const uint16_t* sVS = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes + 2 * L.sc_bytes) + lr0 * NG;
       [[maybe_unused]] const uint16_t* sVB = reinterpret_cast<const uint16_t*>(st + 2 * L.codes_bytes + 3 * L.sc_bytes) + lr0 * NG;
 
-      // ---- phase 0: per-(row, group) coefficients of K and V (a fixed trip count, so all the loads issue at once)
-      constexpr int P0 = (R * NG + 31) / 32;
+      // ---- phase 0: per-(row, group) coefficients of K and V (a fixed trip count, so all the loads issue at once).
+      // Blocks with more (row, group) pairs than lanes take two groups of a row per lane and load (NG is even and a
+      // row's scales start on a 4-byte boundary); smaller ones one pair per lane.
+      constexpr bool PAIRS = R * NG > 32;
+      constexpr int P0 = PAIRS ? (R * NG / 2 + 31) / 32 : 1;
 #pragma unroll
-      for (int it = 0; it < P0; ++it) {
+      for (int it = 0; it < P0 && !PAIRS; ++it) {
         const int idx = lane + 32 * it;
         if (idx < rows_valid * NG) {
           const float2 ak = coeffs<BITS, EXACT_K>(half_bits_to_float_rt(sKS[idx], f16), half_bits_to_float_rt(sKB[idx], f16));
@@ -340,6 +359,23 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
             const float2 av = coeffs<BITS, EXACT>(half_bits_to_float_rt(sVS[idx], f16), half_bits_to_float_rt(sVB[idx], f16));
             sAV[idx] = av.x;
             sBV[idx] = av.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < P0 && PAIRS; ++it) {
+        const int i2 = lane + 32 * it;   // groups 2 * i2 and 2 * i2 + 1 of the block's flattened (row, group) list
+        if (i2 < rows_valid * (NG / 2)) {
+          float2 A, B;
+          coeffs2<BITS, EXACT_K>(half2_bits_to_float2_rt(reinterpret_cast<const uint32_t*>(sKS)[i2], f16),
+                                 half2_bits_to_float2_rt(reinterpret_cast<const uint32_t*>(sKB)[i2], f16), A, B);
+          reinterpret_cast<float4*>(sAB)[2 * i2] = make_float4(A.x, A.x, B.x, B.x);
+          reinterpret_cast<float4*>(sAB)[2 * i2 + 1] = make_float4(A.y, A.y, B.y, B.y);
+          if constexpr (!STATS) {
+            coeffs2<BITS, EXACT>(half2_bits_to_float2_rt(reinterpret_cast<const uint32_t*>(sVS)[i2], f16),
+                                 half2_bits_to_float2_rt(reinterpret_cast<const uint32_t*>(sVB)[i2], f16), A, B);
+            reinterpret_cast<float2*>(sAV)[i2] = A;
+            reinterpret_cast<float2*>(sBV)[i2] = B;
           }
         }
       }
