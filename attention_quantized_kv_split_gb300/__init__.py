@@ -66,6 +66,22 @@ def qdecode_attn_noalloc(q: torch.Tensor, k_packed: torch.Tensor, k_scales: torc
     return out
 
 
+def qdecode_attn_host(q: torch.Tensor, k_packed: torch.Tensor, k_scales: torch.Tensor, k_biases: torch.Tensor,
+                      v_packed: torch.Tensor, v_scales: torch.Tensor, v_biases: torch.Tensor, out: torch.Tensor,
+                      N: Sequence[int], Hkv: int, GS: int, bits: int, stream=None) -> torch.Tensor:
+    """qdecode_attn with every tensor in HOST memory (contiguous CPU tensors; pinned ones copy at full speed): the
+    library stages the inputs on the current device, decodes and copies out back, asynchronously on `stream`.
+    Synchronise the stream before reading out or changing the inputs."""
+    ts = (q, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, out)
+    if any(t.is_cuda or not t.is_contiguous() for t in ts):
+        raise ValueError("qdecode_attn_host takes contiguous host tensors")
+    B, H, D = q.shape
+    st = lib().qdecode_attn_host(*(_ptr(t) for t in ts), B, H, Hkv, _lib.int32_array(N), D, GS, bits,
+                                 dtype_code(q.dtype, out.dtype), _stream(stream))
+    _lib.check(st, "qdecode_attn_host")
+    return out
+
+
 def qdecode_attn_compat(q: torch.Tensor, k_packed: torch.Tensor, k_scales: torch.Tensor, k_biases: torch.Tensor,
                         v_packed: torch.Tensor, v_scales: torch.Tensor, v_biases: torch.Tensor, out: torch.Tensor,
                         N: Sequence[int], Hkv: int, GS: int, bits: int, stream=None) -> torch.Tensor:

@@ -48,6 +48,7 @@ _PI32 = ctypes.POINTER(ctypes.c_int32)
 SIGNATURES = {
     "qdecode_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _PI32, _I, _I, _I, _I, _P]),
     "qdecode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _PI32, _I, _I, _I, _I, _P]),
+    "qdecode_attn_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _PI32, _I, _I, _I, _I, _P]),
     "qdecode_attn_compat": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _PI32, _I, _I, _I, _I, _P]),
     "qdecode_attn_multi": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _PI32, _I, _I, _I, _I, _P]),
     "qdecode_attn_multi_plan": (_I, [_I, _I, _I, _I, _PI32, _I, _I, _I, _I, _I, ctypes.POINTER(QdaPlan)]),

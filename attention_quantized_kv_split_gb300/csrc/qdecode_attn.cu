@@ -37,6 +37,19 @@ struct DeviceState {
 };
 DeviceState g_dev[kMaxDevices];
 
+// Staging of the host-buffer entry point on one device: two sets of device buffers used in turn, so that one call's
+// host->device copies (on the library's copy stream) overlap the previous call's kernels (on the caller's stream).
+struct HostStage {
+  std::mutex mu;
+  cudaStream_t copy = nullptr;
+  cudaEvent_t copied[2] = {nullptr, nullptr};    // set i holds this call's inputs
+  cudaEvent_t released[2] = {nullptr, nullptr};  // the last work that read set i (kernels, output copy) is done
+  void* buf[2] = {nullptr, nullptr};
+  size_t bytes[2] = {0, 0};
+  int turn = 0;
+};
+HostStage g_stage[kMaxDevices];
+
 int cuda_fail(cudaError_t e) {
   t_last_cuda_error = (int)e;
   return QDA_ERR_CUDA;
@@ -458,6 +471,74 @@ int qdecode_attn_noalloc(const void* q, const uint32_t* k_packed, const void* k_
                          int H, int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream) {
   return run_call(q, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, out, B, 1, H, Hkv, N, D, GS, bits,
                   dtype, stream, Scratch::kStatic);
+}
+
+// Host buffers in and out: stage the inputs on the device, decode, copy the output back (all asynchronous).
+int qdecode_attn_host(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
+                      const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out, int B, int H,
+                      int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream) {
+  if (!q || !k_packed || !k_scales || !k_biases || !v_packed || !v_scales || !v_biases || !out)
+    return QDA_ERR_INVALID;
+  int in_dt, out_dt;
+  int st = check_dtype(dtype, &in_dt, &out_dt);
+  if (st != QDA_OK) return st;
+  st = check_shape(B, 1, H, Hkv, N, D, GS, bits);
+  if (st != QDA_OK) return st;
+  int dev;
+  DeviceState* d = device_state(&dev);
+  if (d == nullptr) return QDA_ERR_CUDA;
+  long long T = 0;
+  for (int b = 0; b < B; ++b) T += (long long)N[b] * Hkv;
+  const size_t in_size = 2, out_size = out_dt == QDA_FP32 ? 4 : 2;
+  // q, K codes, K scales, K biases, V codes, V scales, V biases, out; each piece 256-byte aligned in the set
+  const size_t sizes[8] = {(size_t)B * H * D * in_size, (size_t)T * (D * bits / 32) * 4, (size_t)T * (D / GS) * 2,
+                           (size_t)T * (D / GS) * 2,    (size_t)T * (D * bits / 32) * 4, (size_t)T * (D / GS) * 2,
+                           (size_t)T * (D / GS) * 2,    (size_t)B * H * D * out_size};
+  size_t offs[9];
+  offs[0] = 0;
+  for (int i = 0; i < 8; ++i) offs[i + 1] = offs[i] + ((sizes[i] + 255) & ~(size_t)255);
+  const void* src[7] = {q, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  HostStage& g = g_stage[dev];
+  std::lock_guard<std::mutex> lock(g.mu);
+  cudaError_t e;
+  if (g.copy == nullptr) {
+    if ((e = cudaStreamCreateWithFlags(&g.copy, cudaStreamNonBlocking)) != cudaSuccess) return cuda_fail(e);
+    for (int i = 0; i < 2; ++i) {
+      if ((e = cudaEventCreateWithFlags(&g.copied[i], cudaEventDisableTiming)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&g.released[i], cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(e);
+    }
+  }
+  const int k = g.turn;
+  if (g.bytes[k] < offs[8]) {
+    // the set may still be read by an earlier call's work: wait for it before freeing
+    if ((e = cudaEventSynchronize(g.released[k])) != cudaSuccess) return cuda_fail(e);
+    if (g.buf[k] != nullptr) cudaFree(g.buf[k]);
+    g.buf[k] = nullptr;
+    g.bytes[k] = 0;
+    if ((e = cudaMalloc(&g.buf[k], offs[8])) != cudaSuccess) return cuda_fail(e);
+    g.bytes[k] = offs[8];
+  }
+  char* base = static_cast<char*>(g.buf[k]);
+  // this set's previous readers are done before its copies overwrite it; then the inputs, then the caller's stream
+  // waits for them
+  if ((e = cudaStreamWaitEvent(g.copy, g.released[k], 0)) != cudaSuccess) return cuda_fail(e);
+  for (int i = 0; i < 7; ++i)
+    if ((e = cudaMemcpyAsync(base + offs[i], src[i], sizes[i], cudaMemcpyHostToDevice, g.copy)) != cudaSuccess)
+      return cuda_fail(e);
+  if ((e = cudaEventRecord(g.copied[k], g.copy)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaStreamWaitEvent(s, g.copied[k], 0)) != cudaSuccess) return cuda_fail(e);
+  st = run_call(base + offs[0], reinterpret_cast<const uint32_t*>(base + offs[1]), base + offs[2], base + offs[3],
+                reinterpret_cast<const uint32_t*>(base + offs[4]), base + offs[5], base + offs[6], base + offs[7], B,
+                1, H, Hkv, N, D, GS, bits, dtype, stream, Scratch::kWorkspace);
+  if (st != QDA_OK) return st;
+  if ((e = cudaMemcpyAsync(out, base + offs[7], sizes[7], cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(e);
+  if ((e = cudaEventRecord(g.released[k], s)) != cudaSuccess) return cuda_fail(e);
+  g.turn = k ^ 1;
+  return QDA_OK;
 }
 
 int qdecode_quantize(const float* x, long long rows, int D, int GS, int bits, int dtype, uint32_t* packed,

@@ -322,26 +322,23 @@ def run_ours(args):
                 "split_kernel_us": round(split_ms * 1e3, 3), "merge_kernel_us": round(merge_ms * 1e3, 3),
                 "algorithmic_bytes_per_launch": nbytes}
 
-    # end to end through the public API with host buffers: H2D of q and the whole cache, the call, D2H of out
+    # end to end through the C ABI with host buffers (qdecode_attn_host): every step copies q and the whole cache from
+    # pinned host memory to the device, decodes, and copies out back; the library overlaps one step's copies with
+    # the previous step's kernels (two staging sets)
     esteps = min(args.steps, 100)
-    hq = q.cpu().pin_memory()
-    host = [t.cpu().pin_memory() for t in (cache.kp, cache.ks, cache.kb, cache.vp, cache.vs, cache.vb)]
-    dev = [torch.empty_like(t) for t in (cache.kp, cache.ks, cache.kb, cache.vp, cache.vs, cache.vb)]
-    dq = torch.empty_like(q)
+    host = [t.cpu().pin_memory() for t in (q, cache.kp, cache.ks, cache.kb, cache.vp, cache.vs, cache.vb)]
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    h2d = hq.numel() * hq.element_size() + sum(t.numel() * t.element_size() for t in host)
+    h2d = sum(t.numel() * t.element_size() for t in host)
     d2h = hout.numel() * hout.element_size()
+    for _ in range(2):   # both staging sets allocated before the timed steps
+        qda.qdecode_attn_host(*host, hout, N, w.Hkv, w.GS, w.bits, stream)
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_push("end-to-end calls (host buffers)")
     e0.record(stream)
     for _ in range(esteps):
-        dq.copy_(hq, non_blocking=True)
-        for d_, h_ in zip(dev, host):
-            d_.copy_(h_, non_blocking=True)
-        qda.qdecode_attn(dq, *dev, out, N, w.Hkv, w.GS, w.bits)
-        hout.copy_(out, non_blocking=True)
+        qda.qdecode_attn_host(*host, hout, N, w.Hkv, w.GS, w.bits, stream)
     e1.record(stream)
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()

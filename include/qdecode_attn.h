@@ -77,6 +77,24 @@ int qdecode_attn(const void* q, const uint32_t* k_packed, const void* k_scales, 
                  int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream);
 
 /*
+ * qdecode_attn_host: qdecode_attn with HOST buffers. q, the six cache arrays and out are host memory in the layouts
+ * above (page-locked memory, e.g. from cudaHostAlloc, gives full-speed asynchronous copies; pageable memory works
+ * and is slower). The call copies q and the cache to a device staging area, decodes with the same kernels as
+ * qdecode_attn, and copies out back, all asynchronously: the result is in out once `stream` has reached the end of
+ * this call's work (cudaStreamSynchronize), and the host inputs must stay unchanged until then. (The pages this
+ * library follows have no counterpart of this entry point; it is the end-to-end path with the cache held on the
+ * host.)
+ *
+ * The staging area is two sets of device buffers owned by the library (allocated or grown with cudaMalloc on first
+ * need, which synchronises the device) that consecutive calls use in turn: one call's host->device copies run on a
+ * library-owned copy stream and overlap the previous call's kernels on `stream`. Calls on one device are
+ * serialised by a lock on the host; the call is not capturable in a CUDA graph. Returns the codes of qdecode_attn.
+ */
+int qdecode_attn_host(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
+                      const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out,
+                      int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int dtype, void* stream);
+
+/*
  * qdecode_attn_noalloc: the same operation, arguments, layouts and result as qdecode_attn, for callers that are not
  * allowed to allocate device memory at all -- for example code running under an allocator that owns the whole
  * device, a real-time loop where cudaMalloc's implicit device synchronisation is not acceptable, or a host that

@@ -275,3 +275,18 @@ def test_cache_append_argument_errors(L):
     assert call(o=[None] * 6) == _lib.QDA_ERR_INVALID             # old rows exist but no old cache
     assert call(x=[None] + out[1:]) == _lib.QDA_ERR_INVALID
     assert call(w=[new[0] + 4, new[1]]) == _lib.QDA_ERR_ALIGN
+
+
+def test_host_entry_argument_errors(L):
+    # the host-buffer entry point checks its arguments like qdecode_attn before touching a device
+    p = [FAKE + 256 * i for i in range(8)]
+    n = _lib.int32_array([64])
+    h = L.qdecode_attn_host
+    assert h(*p, 1, 8, 2, n, 96, 32, 4, 1, None) == _lib.QDA_ERR_UNSUPPORTED
+    assert h(*p, 1, 8, 3, n, 256, 32, 4, 1, None) == _lib.QDA_ERR_INVALID
+    assert h(*p, 1, 8, 2, n, 256, 32, 5, 1, None) == _lib.QDA_ERR_UNSUPPORTED
+    assert h(*p, 1, 8, 2, n, 256, 32, 4, 7, None) == _lib.QDA_ERR_INVALID
+    assert h(*p, 1, 8, 2, _lib.int32_array([0]), 256, 32, 4, 1, None) == _lib.QDA_ERR_INVALID
+    q = list(p)
+    q[7] = None
+    assert h(*q, 1, 8, 2, n, 256, 32, 4, 1, None) == _lib.QDA_ERR_INVALID
