@@ -108,7 +108,8 @@ cudaError_t qda_occupancy_split2_b8_x1(int D, int nh, int ng, size_t smem, int* 
 // Records a CUDA runtime error for qdecode_attn_last_cuda_error() (this host thread) and returns QDA_ERR_CUDA.
 int qda_cuda_fail(cudaError_t e);
 
-cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool pdl, cudaStream_t s);
+// slices: CTAs per (b, l, h), each combining D / slices values of the head dimension.
+cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool pdl, int slices, cudaStream_t s);
 
 // Where the quantizer writes its rows. append = 0: row i to row i. append = 1 (cache append): input row
 // i = ((b * Hkv) + kvh) * T + t goes to row Hkv * off_new[b] + kvh * (n_old[b] + T) + n_old[b] + t of the new cache,

@@ -35,13 +35,14 @@ __device__ __forceinline__ void store4(void* out, size_t idx, float4 v) {
 }
 
 // out[b, l, h, :] = sum_s o_s 2^(m_s - M) / sum_s l_s 2^(m_s - M) over the partial slots of (b, KV head of h)
-// (mlx-bun fused-decode-kernel.ts, MERGE_SOURCE), in log2 units. One CTA per (b, l, h); l is the query position
-// (always 0 for single-query decode). A slot whose rows were all hidden from the head holds m = -inf and is
-// skipped. In compat mode (the two-pass form) the partials already carry normalised weights and are only summed
-// (in the same fixed order): out = T(sum_s o_s). The slots are dealt to
-// kMergeThreads / (D/4) thread groups round-robin; each thread folds its slots in one pass with a running max, so
-// the (m, l) and o loads of a slot are issued together, and the groups are then combined in a fixed order:
-// deterministic, no atomics.
+// (mlx-bun fused-decode-kernel.ts, MERGE_SOURCE), in log2 units. One CTA per (b, l, h) and slice of the head
+// dimension (gridDim.y slices; one, or 64 values each when a head has many slots); l is the query position
+// (always 0 for single-query decode). A slot whose rows were all hidden
+// from the head holds m = -inf and is skipped. In compat mode (the two-pass form) the partials already carry
+// normalised weights and are only summed (in the same fixed order): out = T(sum_s o_s). The slots are dealt to
+// kMergeThreads / (slice / 4) thread groups round-robin (4 values per thread); each thread folds its slots
+// in one pass with a running max, so the (m, l) and o loads of a slot are issued together, and the groups are then
+// combined in a fixed order: deterministic, no atomics.
 constexpr int kMergeThreads = 512;
 
 template <int OUT>
@@ -63,9 +64,11 @@ __global__ void __launch_bounds__(kMergeThreads) qda_merge_kernel(const __grid_c
   const int cf = qda_cta_of(T, C, us);
   const int ns = qda_cta_of(T, C, us + n - 1) - cf + 1;
   const bool maybe_empty = T / C < 8;   // only ranges shorter than 8 rows can be empty (and wrote no slot)
-  const int tpr = D >> 2;
+  // this CTA's slice of the head dimension (gridDim.y slices of D / gridDim.y values), 4 values per thread
+  const int dims = D / (int)gridDim.y;
+  const int tpr = dims >> 2;
   const int groups = kMergeThreads / tpr;
-  const int grp = tid / tpr, t = tid - grp * tpr;
+  const int grp = tid / tpr, t = (int)blockIdx.y * tpr + (tid - grp * tpr);
 
   pdl_wait();   // the split kernel's partials are complete and visible from here on
 
@@ -93,7 +96,7 @@ __global__ void __launch_bounds__(kMergeThreads) qda_merge_kernel(const __grid_c
     m_run = mn;
   }
   red_o[tid] = acc;
-  if (t == 0) red_ml[grp] = make_float2(m_run, den);
+  if (tid - grp * tpr == 0) red_ml[grp] = make_float2(m_run, den);
   __syncthreads();
   if (grp != 0) return;
   float M = -INFINITY;
@@ -104,7 +107,7 @@ __global__ void __launch_bounds__(kMergeThreads) qda_merge_kernel(const __grid_c
     const float2 ml = red_ml[g];
     if (ml.x == -INFINITY) continue;   // a group that held no slot
     const float w = ex2m(ml.x - M);
-    const float4 v = red_o[g * tpr + t];
+    const float4 v = red_o[g * tpr + tid];
     dt = fmaf(ml.y, w, dt);
     o.x = fmaf(v.x, w, o.x);
     o.y = fmaf(v.y, w, o.y);
@@ -276,9 +279,10 @@ cudaError_t launch_quant(const float* x, long long rows, int D, int GS, uint32_t
 
 }  // namespace qda
 
-cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool pdl, cudaStream_t s) {
+cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool pdl, int slices, cudaStream_t s) {
+  if (slices < 1 || p.D % (4 * slices) != 0 || p.D / 4 / slices > qda::kMergeThreads) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.B * p.L * p.H));
+  cfg.gridDim = dim3((unsigned)(p.B * p.L * p.H), (unsigned)slices);
   cfg.blockDim = dim3(qda::kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;

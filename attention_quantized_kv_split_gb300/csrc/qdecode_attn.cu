@@ -386,7 +386,13 @@ int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, cons
     e = cudaEventRecord(static_cast<cudaEvent_t>(t_split_event), s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  e = qda_launch_merge(p, out, out_dt, !use_event, s);
+  // a head whose partials span many slots is merged by D / 64 CTAs (one per 64 values) instead of one: about
+  // slots * D / 2048 dependent slot loads per thread group of one CTA, more than 6 leave the merge latency-bound
+  int max_n = 0;
+  for (int b = 0; b < B; ++b) max_n = std::max(max_n, (int)N[b]);
+  const long long slots = (long long)max_n * plan.num_ctas / std::max(1LL, plan.total_rows) + 2;
+  const int slices = (D >= 128 && slots * D > 6LL * 2048) ? D / 64 : 1;
+  e = qda_launch_merge(p, out, out_dt, !use_event, slices, s);
   if (e != cudaSuccess) return cuda_fail(e);
   g_calls.fetch_add(1);
   return QDA_OK;
