@@ -10,6 +10,7 @@
 
 #define QDA_NW 4                         // consumer warps per CTA of the split kernel
 #define QDA_THREADS ((QDA_NW + 1) * 32)  // + one producer warp that drives the bulk copies
+#define QDA_SPLIT2_TILE 64                // rows per pipeline stage of the lean split kernel
 
 // Launch parameters of the split and merge kernels (passed by value as a __grid_constant__).
 struct QdaParams {

@@ -151,7 +151,8 @@ struct Split2Geom {
   static constexpr int KW = EK * BITS / 32;     // K words per lane per row
   static constexpr int VW = EV * BITS / 32;     // V words per lane per row
   static constexpr int W = D * BITS / 32;       // words per row
-  static constexpr int TILE = R * QDA_NW;       // rows per pipeline stage
+  static constexpr int TILE = QDA_SPLIT2_TILE;  // rows per pipeline stage (TILE / R blocks, dealt to the warps)
+  static_assert(TILE % (R * QDA_NW) == 0, "every warp takes the same number of blocks of a full chunk");
   static_assert(NVL >= 1, "reduction must end with at least one score per lane");
 };
 
@@ -176,7 +177,8 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
   constexpr float LOG2E = 1.4426950408889634f;
 
   extern __shared__ __align__(1024) unsigned char smem[];
-  const int TILE = p.tile_rows, STAGES = p.stages;
+  constexpr int TILE = G::TILE;   // the host plans this kernel with this tile (stage offsets are constants)
+  const int STAGES = p.stages;
   const bool f16 = p.f16 != 0;
   const QdaSmemLayout L = qda_smem_layout(TILE, STAGES, W, NG, NH, D);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);

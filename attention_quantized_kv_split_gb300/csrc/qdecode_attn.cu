@@ -118,7 +118,7 @@ Variant pick_variant(int nrep, int D, int GS, int bits) {
     v.hc = (nrep + v.nh - 1) / v.nh;
     v.heads_pad = v.hc * v.nh;
     const int R = split2_rows(D, v.nh);
-    v.tile = std::max(64, R * QDA_NW);   // warps take TILE / R blocks of a chunk in turn
+    v.tile = QDA_SPLIT2_TILE;   // warps take TILE / R blocks of a chunk in turn (the kernel's constant tile)
     const QdaSmemLayout L = qda_smem_layout(v.tile, 1, v.W, v.NG, v.nh, D);
     const size_t scratch = (size_t)QDA_NW * split2_scratch_floats(R, v.NG, v.nh) * 4;
     const size_t comb = (size_t)QDA_NW * v.nh * D * 4 + (size_t)QDA_NW * v.nh * 2 * 4;
