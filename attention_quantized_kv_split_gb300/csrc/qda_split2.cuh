@@ -177,7 +177,10 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
   constexpr float LOG2E = 1.4426950408889634f;
 
   extern __shared__ __align__(1024) unsigned char smem[];
-  constexpr int TILE = G::TILE;   // the host plans this kernel with this tile (stage offsets are constants)
+  // the host plans this kernel with a 64-row tile; the 4-head and D = 512 kernels take it as a constant (every
+  // stage and block offset folds, which frees registers), the 2-head D = 256 ones from the parameters (measured
+  // faster there)
+  const int TILE = (NH == 4 || D == 512) ? G::TILE : p.tile_rows;
   const int STAGES = p.stages;
   const bool f16 = p.f16 != 0;
   const QdaSmemLayout L = qda_smem_layout(TILE, STAGES, W, NG, NH, D);
