@@ -359,7 +359,7 @@ def run_ours(args):
                 fx()
             msx = time_calls(fx, 50, flush, stream)
             bx = kv_bytes(wx, Nx)
-            mx = statistics.median(msx)
+            mx = statistics.mean(msx)
             extra[wx.name] = {"us_per_call": round(mx * 1e3, 2), "kv_GBps": round(bx / (mx * 1e-3) / 1e9, 1),
                               "frac_of_peak": round(bx / (mx * 1e-3) / 1e9 / peak, 4), "kv_bytes": bx}
             del cx, qx, ox
@@ -371,7 +371,7 @@ def run_ours(args):
                                                     N, w.Hkv, w.GS, w.bits, stream)
             for _ in range(5):
                 ccall()
-            mc = statistics.median(time_calls(ccall, 50, flush, stream))
+            mc = statistics.mean(time_calls(ccall, 50, flush, stream))
             extra[f"{w.name}_two_pass_compat"] = {
                 "us_per_call": round(mc * 1e3, 2), "kv_GBps": round(nbytes / (mc * 1e-3) / 1e9, 1),
                 "frac_of_peak": round(nbytes / (mc * 1e-3) / 1e9 / peak, 4), "kv_bytes": nbytes,
@@ -388,7 +388,7 @@ def run_ours(args):
         gcall = lambda: qda.qdecode_qgemv(gx, gw, gs, gb, gy, gGS, 8, stream)
         for _ in range(5):
             gcall()
-        mg = statistics.median(time_calls(gcall, 50, flush, stream))
+        mg = statistics.mean(time_calls(gcall, 50, flush, stream))
         gbytes = gN * gK + 2 * 2 * gN * (gK // gGS)
         extra["qgemv_8b_K4096_N14336_T1_GS64_bf16"] = {
             "us_per_call": round(mg * 1e3, 2), "GBps": round(gbytes / (mg * 1e-3) / 1e9, 1),
@@ -401,7 +401,7 @@ def run_ours(args):
         acall = lambda: cache.append(akn, avn, out=anext, stream=stream)
         for _ in range(5):
             acall()
-        ma = statistics.median(time_calls(acall, 50, flush, stream))
+        ma = statistics.mean(time_calls(acall, 50, flush, stream))
         abytes = nbytes + anext.nbytes()   # old cache read once, new cache written once
         extra[f"{w.name}_append_1_token"] = {
             "us_per_call": round(ma * 1e3, 2), "GBps": round(abytes / (ma * 1e-3) / 1e9, 1),
@@ -419,7 +419,7 @@ def run_ours(args):
         for _ in range(5):
             gcall2()
         torch.cuda.synchronize()
-        mgr = statistics.median(time_calls(gcall2, 50, flush, torch.cuda.current_stream()))
+        mgr = statistics.mean(time_calls(gcall2, 50, flush, torch.cuda.current_stream()))
         extra[f"{w.name}_graph_replay"] = {"us_per_call": round(mgr * 1e3, 2),
                                            "kv_GBps": round(nbytes / (mgr * 1e-3) / 1e9, 1),
                                            "frac_of_peak": round(nbytes / (mgr * 1e-3) / 1e9 / peak, 4)}
@@ -432,7 +432,7 @@ def run_ours(args):
                                                N, w.Hkv, w.GS, w.bits, stream)
         for _ in range(5):
             mcall()
-        mm = statistics.median(time_calls(mcall, 50, flush, stream))
+        mm = statistics.mean(time_calls(mcall, 50, flush, stream))
         extra[f"{w.name}_L{Lq}"] = {"us_per_call": round(mm * 1e3, 2), "kv_GBps": round(nbytes / (mm * 1e-3) / 1e9, 1),
                                     "frac_of_peak": round(nbytes / (mm * 1e-3) / 1e9 / peak, 4), "kv_bytes": nbytes,
                                     "query_positions": Lq}
