@@ -87,6 +87,20 @@ def test_forced_splits_within_tolerance(splits):
     assert torch.equal(out1, out2)
 
 
+@pytest.mark.parametrize("D,GS,out", [(128, 32, "fp32"), (512, 64, None), (512, 128, "fp32")])
+def test_merge_over_head_dimension_slices(D, GS, out):
+    # enough forced splits that every head's partials span many slots: the merge then runs one CTA per 64 values of
+    # the head dimension (D / 64 CTAs per head); the result must still match the oracle and repeat bit for bit
+    w = synth.small(B=2, H=8, Hkv=2, D=D, N=(1500, 37), bits=4, GS=GS, dtype_out=out or "bf16", seed=D + GS)
+    out1, (q, dev, N) = check_small(w, splits=600)
+    qda.qdecode_attn_debug_force_splits(600)
+    try:
+        out2 = run_gpu(q, dev, N, w)
+    finally:
+        qda.qdecode_attn_debug_force_splits(0)
+    assert torch.equal(out1, out2)
+
+
 def test_run_to_run_bitwise_identical():
     w = synth.small(B=4, H=16, Hkv=4, D=256, N=(3000, 20, 1, 9000), bits=4, GS=64, seed=21)
     q, cache, N = small_case(w)
