@@ -25,6 +25,7 @@ struct QdaParams {
   float2* part_ml;            // [slots, heads_pad] (running max in log2 units, sum of 2^(s - max))
   unsigned int* err;          // device error word
   long long total_rows;       // T = Hkv * sum(N)
+  unsigned long long cta_magic;   // ceil(2^64 / num_ctas): qda_cta_row_fast divides by num_ctas with it
   int B, H, Hkv, D, GS, NG, W, nrep, heads_pad, head_chunks, num_ctas, tile_rows, stages;
   int L;                      // query positions per sequence; head j of a KV head is (position j / nrep, j % nrep)
   int mode;                   // lean split kernel: 0 single-pass, 1 multi-query, 2 compat pass A, 3 compat pass B
@@ -51,6 +52,22 @@ __host__ __device__ inline long long qda_cta_row(long long T, int C, int c) {
   if (c >= C) return T;
   if (c <= 0) return 0;
   return ((T * (long long)c) / C) & ~7LL;
+}
+
+// qda_cta_row with the division by C done as a multiply by magic = ceil(2^64 / C) (the high half of the 128-bit
+// product). Exact while T * c < 2^52 and C <= 4096: the product overshoots (T * c) / C by less than
+// T * c / 2^64 < 2^-12 <= 1 / C, too little to reach the next integer. T < 2^37 here (int32 sequence offsets,
+// at most 64 KV heads) and C <= 4096 (the plan's cap).
+__host__ __device__ inline long long qda_cta_row_fast(long long T, int C, unsigned long long magic, int c) {
+  if (c >= C) return T;
+  if (c <= 0) return 0;
+  const unsigned long long x = (unsigned long long)T * (unsigned long long)c;
+#ifdef __CUDA_ARCH__
+  const unsigned long long q = __umul64hi(x, magic);
+#else
+  const unsigned long long q = (unsigned long long)(((unsigned __int128)x * magic) >> 64);
+#endif
+  return (long long)q & ~7LL;
 }
 
 // CTA whose row range holds row r (empty ranges are skipped).

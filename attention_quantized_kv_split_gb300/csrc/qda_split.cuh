@@ -83,7 +83,8 @@ struct ChunkWalker {
     b = lo;
     const long long n = p.seq_off[b + 1] - p.seq_off[b];
     const long long sb = (long long)p.Hkv * p.seq_off[b];
-    kvh = (int)((r0 - sb) / n);
+    const long long off = r0 - sb;   // < Hkv * n; a 32-bit division when it fits
+    kvh = off < (1LL << 31) ? (int)((unsigned)off / (unsigned)n) : (int)(off / n);
     u_start = sb + (long long)kvh * n;
     u_end = u_start + n;
     unit = b * p.Hkv + kvh;
@@ -230,8 +231,8 @@ __global__ void __launch_bounds__(QDA_THREADS) qda_split_kernel(const __grid_con
   // head chunks of one row range are adjacent blocks, so a second chunk re-reads rows while they are in L2
   const int cta = blockIdx.x / p.head_chunks, hc = blockIdx.x - cta * p.head_chunks;
   const long long T = p.total_rows;
-  const long long r0 = qda_cta_row(T, p.num_ctas, cta);
-  const long long r1 = qda_cta_row(T, p.num_ctas, cta + 1);
+  const long long r0 = qda_cta_row_fast(T, p.num_ctas, p.cta_magic, cta);
+  const long long r1 = qda_cta_row_fast(T, p.num_ctas, p.cta_magic, cta + 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {

@@ -196,8 +196,8 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
   // head chunks of one row range are adjacent blocks, so a second chunk re-reads rows while they are in L2
   const int cta = blockIdx.x / p.head_chunks, hc = blockIdx.x - cta * p.head_chunks;
   const long long T = p.total_rows;
-  const long long r0 = qda_cta_row(T, p.num_ctas, cta);
-  const long long r1 = qda_cta_row(T, p.num_ctas, cta + 1);
+  const long long r0 = qda_cta_row_fast(T, p.num_ctas, p.cta_magic, cta);
+  const long long r1 = qda_cta_row_fast(T, p.num_ctas, p.cta_magic, cta + 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {

@@ -342,6 +342,7 @@ int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, cons
   p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + ((o_bytes + 255) & ~(size_t)255));
   p.err = d->err;
   p.total_rows = plan.total_rows;
+  p.cta_magic = ~0ULL / (unsigned long long)plan.num_ctas + 1ULL;
   p.B = B;
   p.L = L;
   p.H = H;

@@ -290,3 +290,21 @@ def test_host_entry_argument_errors(L):
     q = list(p)
     q[7] = None
     assert h(*q, 1, 8, 2, n, 256, 32, 4, 1, None) == _lib.QDA_ERR_INVALID
+
+
+def test_cta_row_magic_division():
+    # the kernels split rows among C CTAs with floor(T * c / C) computed as the high half of (T * c) * ceil(2^64 / C);
+    # that must equal the exact quotient for every CTA count the plan can choose (1..4096) and every row total the
+    # argument checks admit (T < 2^37: int32 sequence offsets times at most 64 KV heads)
+    import random
+    rng = random.Random(5)
+    Ts = [1, 7, 8, 4095, 4096, 65536, (1 << 31) - 1, (1 << 37) - 1, (1 << 37) - 4096] + \
+         [rng.randrange(1, 1 << 37) for _ in range(40)]
+    for C in list(range(1, 4097)):
+        m = ((1 << 64) - 1) // C + 1
+        for T in (Ts if C % 97 == 0 or C < 64 or C > 4000 else Ts[:4] + Ts[-3:]):
+            for c in {1, C - 1, C // 2, rng.randrange(1, C + 1)}:
+                if c <= 0 or c >= C:
+                    continue
+                x = T * c
+                assert (x * m) >> 64 == x // C, (T, C, c)
