@@ -85,6 +85,12 @@ def test_compat_forced_splits(splits):
     check(synth.small(B=3, H=8, Hkv=2, D=256, N=(500, 9, 1500), bits=4, GS=32, seed=splits), splits=splits)
 
 
+def test_compat_maximum_batch():
+    # QDA_MAX_B sequences of 1-6 rows: pass B folds pass A's statistics for 1024 units, most of them inside one range
+    N = tuple(1 + (b * 5) % 6 for b in range(512))
+    check(synth.small(B=len(N), H=4, Hkv=2, D=256, N=N, bits=8, GS=64, seed=13))
+
+
 def test_compat_run_to_run_bitwise():
     w = synth.small(B=2, H=16, Hkv=8, D=256, N=(4000, 333), bits=8, GS=32, seed=41)
     out1, (q, dev, N) = check(w)

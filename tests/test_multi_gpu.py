@@ -63,7 +63,7 @@ def test_multi_shape_sweep(D, bits, GS, L):
     check(synth.small(B=2, H=4, Hkv=2, D=D, N=(131, L), bits=bits, GS=GS, seed=D * 3 + bits + GS + L), L)
 
 
-@pytest.mark.parametrize("H,Hkv,L", [(8, 2, 4), (16, 8, 4), (16, 4, 2), (3, 1, 3), (32, 8, 2), (4, 4, 8)])
+@pytest.mark.parametrize("H,Hkv,L", [(8, 2, 4), (16, 8, 4), (16, 4, 2), (3, 1, 3), (32, 8, 2), (4, 4, 8), (8, 1, 8)])
 def test_multi_gqa_and_positions(H, Hkv, L):
     check(synth.small(B=2, H=H, Hkv=Hkv, D=256, N=(300, 41), bits=4, GS=64, seed=H * 7 + Hkv + L), L)
 

@@ -10,7 +10,7 @@ import torch
 
 import oracle as O
 import attention_quantized_kv_split_gb300 as qda
-from attention_quantized_kv_split_gb300 import build, synth
+from attention_quantized_kv_split_gb300 import _lib as qlib, build, synth
 
 from harness import (TORCH_DT, compare, gpu_quantized_workload, oracle_out, run_gpu, small_case,
                      unit_oracle_cache, upload_cache)
@@ -67,6 +67,19 @@ def test_dtypes(dt_in, dt_out):
 
 def test_ragged_batch():
     check_small(synth.small(B=5, H=8, Hkv=4, D=256, N=(1, 17, 300, 8, 1025), bits=4, GS=64, seed=3))
+
+
+def test_maximum_batch_of_tiny_sequences():
+    # QDA_MAX_B sequences of 1-6 rows: 1024 (sequence, KV head) units, so every CTA range crosses dozens of unit
+    # boundaries (one partial slot per segment) and the merge covers 4096 heads
+    N = tuple(1 + (b * 5) % 6 for b in range(qlib.QDA_MAX_B))
+    check_small(synth.small(B=len(N), H=8, Hkv=2, D=256, N=N, bits=4, GS=64, seed=11))
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_maximum_query_heads_per_kv_head(D):
+    # QDA_MAX_NREP query heads share one KV head (the lean kernel takes them 4 at a time in 16 head chunks)
+    check_small(synth.small(B=1, H=qlib.QDA_MAX_NREP, Hkv=1, D=D, N=(300,), bits=8, GS=32, seed=D + 64))
 
 
 def test_ragged_tail_scale_bytes():
