@@ -221,15 +221,36 @@ def cpu_baseline(w, N, q, cache, pool):
                       f"one single-threaded worker process per unit", "seconds": dt}
 
 
+def ranks_from_env():
+    """(world size, rank, local rank) of this process under torchrun, (1, 0, 0) alone."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest x over the ranks of the default process group (the slowest replica sets the job's time). The
+    tensor lives on `device` (a CUDA device for NCCL, the CPU for gloo)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(world: int, nbytes: int, steps: int, max_ms_total: float) -> float:
+    """Replicas: every rank moves nbytes per step, the job's time is the slowest rank's."""
+    return world * nbytes * steps / (max_ms_total * 1e-3) / 1e9
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
     import attention_quantized_kv_split_gb300 as qda
     from attention_quantized_kv_split_gb300 import build, synth
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = ranks_from_env()
     pool = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # the oracle's worker pool is spawned before the first GPU call
@@ -283,14 +304,10 @@ def run_ours(args):
     clocks = sampler.summary(t0, t1) if sampler else None
     if sampler:
         sampler.stop()
-    dev_ms_total = sum(ms)
-    if world > 1:
-        tt = torch.tensor([dev_ms_total], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        dev_ms_total = float(tt.item())
+    dev_ms_total = max_over_ranks(sum(ms), world, device)
     nbytes = kv_bytes(w, N)
     ms_per_step = dev_ms_total / args.steps
-    value = world * nbytes * args.steps / (dev_ms_total * 1e-3) / 1e9
+    value = whole_job_gbps(world, nbytes, args.steps, dev_ms_total)
 
     if rank != 0:
         if world > 1:
