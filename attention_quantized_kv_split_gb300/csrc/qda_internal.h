@@ -103,8 +103,9 @@ __host__ __device__ inline QdaSmemLayout qda_smem_layout(int tile_rows, int stag
 // Lean split kernel: floats of per-warp scratch (K coefficients (A, A, B, B) and V coefficients A_v, B_v per
 // (row, group), p * A_v pairs per (row, head, group) with one float4 of padding per row, per-head sums of p * B_v
 // per group).
+// Rounded up to whole float4s: every warp's scratch starts on a 16-byte boundary (its first array is read as float4).
 __host__ __device__ inline int split2_scratch_floats(int R, int NG, int NH) {
-  return R * NG * (4 + 2) + R * ((NH / 2) * NG + 1) * 4 + NH * NG;
+  return (R * NG * (4 + 2) + R * ((NH / 2) * NG + 1) * 4 + NH * NG + 3) & ~3;
 }
 
 // Launchers of the split kernels, one translation unit per (kernel, bits[, exact]). They return cudaSuccess or the
@@ -122,6 +123,15 @@ cudaError_t qda_occupancy_split2_b4_x0(int D, int nh, int ng, size_t smem, int* 
 cudaError_t qda_occupancy_split2_b4_x1(int D, int nh, int ng, size_t smem, int* ctas_per_sm);
 cudaError_t qda_occupancy_split2_b8_x0(int D, int nh, int ng, size_t smem, int* ctas_per_sm);
 cudaError_t qda_occupancy_split2_b8_x1(int D, int nh, int ng, size_t smem, int* ctas_per_sm);
+// the D = 64 and 128 instances of the lean kernel (their own translation units)
+cudaError_t qda_launch_split2s_b4_x0(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem, cudaStream_t s);
+cudaError_t qda_launch_split2s_b4_x1(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem, cudaStream_t s);
+cudaError_t qda_launch_split2s_b8_x0(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem, cudaStream_t s);
+cudaError_t qda_launch_split2s_b8_x1(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem, cudaStream_t s);
+cudaError_t qda_occupancy_split2s_b4_x0(int D, int nh, int ng, size_t smem, int* ctas_per_sm);
+cudaError_t qda_occupancy_split2s_b4_x1(int D, int nh, int ng, size_t smem, int* ctas_per_sm);
+cudaError_t qda_occupancy_split2s_b8_x0(int D, int nh, int ng, size_t smem, int* ctas_per_sm);
+cudaError_t qda_occupancy_split2s_b8_x1(int D, int nh, int ng, size_t smem, int* ctas_per_sm);
 
 // Records a CUDA runtime error for qdecode_attn_last_cuda_error() (this host thread) and returns QDA_ERR_CUDA.
 int qda_cuda_fail(cudaError_t e);

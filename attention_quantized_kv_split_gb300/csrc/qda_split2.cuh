@@ -1,4 +1,5 @@
-// Split kernel, arithmetic-lean variant: D = 256 with 2 or 4 query heads per CTA, D = 512 with 2 (sm_103a).
+// Split kernel, arithmetic-lean variant: D = 64, 128 and 256 with 2 or 4 query heads per CTA, D = 512 with 2
+// (sm_103a).
 //
 // Same data path as qda_split_kernel (one contiguous row range per CTA, producer warp + bulk copies into a
 // shared-memory ring, one partial per (segment, query head)), but the consumer warps are organised around the
@@ -8,8 +9,10 @@
 //     output needs it; the constant offset is folded into per-row coefficients A, B with
 //     s*c + b = A*f + B, computed once per (row, group) by the warp before its rows are used;
 //   * every dot product and every V update is a packed two-lane FMA (f32x2);
-//   * K rows are read by 16 lanes (16 codes each) and the per-row sums are formed by a transposed butterfly,
+//   * K rows are read by D/16 lanes (16 codes each) and the per-row sums are formed by a transposed butterfly,
 //     so each lane ends with whole scores for fixed (rows, head) instead of every lane reducing every score;
+//   * V rows are read by 32 lanes (D/32 codes each), or at D = 128 and 64 by 16 and 8 lanes of 8 codes, which then
+//     take 2 and 4 rows a step and add their sums at the segment end;
 //   * the online softmax advances once per block of R rows per warp (one max, one rescale of o when it moves);
 //   * the lane that owns a score also forms p * A_v for every group of that row (the V coefficient of the
 //     mlx-bun SCORE_ROW factoring, applied to V) and keeps the sum of p * B_v, so the V lanes only load them.
@@ -141,19 +144,22 @@ __device__ __forceinline__ void load_words(const uint32_t* src, uint32_t (&w)[N]
 template <int BITS, int D, int NH>
 struct Split2Geom {
   static constexpr int EK = 16;                 // K codes per lane per row
-  static constexpr int LK = D / EK;             // lanes per K row (16 or 32)
+  static constexpr int LK = D / EK;             // lanes per K row (4, 8, 16 or 32)
   static constexpr int RPS = 32 / LK;           // K rows per warp step
   static constexpr int R = NH == 4 ? 8 : 16;  // rows per warp block (fewer live scores with 4 heads)
   static constexpr int S = R / RPS;             // K steps per block
   static constexpr int NV = NH * S;             // partial scores per lane before the reduction
   static constexpr int NVL = NV / LK;           // scores per lane after it
-  static constexpr int EV = D / 32;             // V codes per lane per row
+  static constexpr int EV = D >= 256 ? D / 32 : 8;   // V codes per lane per row (at least one word of 4-bit codes)
+  static constexpr int VL = D / EV;             // lanes per V row (32, or 16 / 8 at D = 128 / 64)
+  static constexpr int VR = 32 / VL;            // V rows per warp step
   static constexpr int KW = EK * BITS / 32;     // K words per lane per row
   static constexpr int VW = EV * BITS / 32;     // V words per lane per row
   static constexpr int W = D * BITS / 32;       // words per row
   static constexpr int TILE = QDA_SPLIT2_TILE;  // rows per pipeline stage (TILE / R blocks, dealt to the warps)
   static_assert(TILE % (R * QDA_NW) == 0, "every warp takes the same number of blocks of a full chunk");
   static_assert(NVL >= 1, "reduction must end with at least one score per lane");
+  static_assert(R % VR == 0, "the V steps cover the block's rows");
 };
 
 // MODE 0: single-pass decode. 1: single-pass with L > 1 query positions (the last L - 1 rows of a unit hidden
@@ -165,10 +171,10 @@ template <int BITS, int D, int NH, int NG, bool EXACT, int MODE>
 __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid_constant__ QdaParams p) {
   using G = Split2Geom<BITS, D, NH>;
   constexpr int EK = G::EK, LK = G::LK, RPS = G::RPS, R = G::R, S = G::S, NV = G::NV, NVL = G::NVL;
-  constexpr int EV = G::EV, KW = G::KW, VW = G::VW, W = G::W;
+  constexpr int EV = G::EV, KW = G::KW, VW = G::VW, W = G::W, VL = G::VL, VR = G::VR;
   constexpr int NW = QDA_NW;
   constexpr int LOG_NH = NH == 4 ? 2 : 1;
-  constexpr int LOG_LK = LK == 32 ? 5 : 4;
+  constexpr int LOG_LK = LK == 32 ? 5 : LK == 16 ? 4 : LK == 8 ? 3 : 2;
   constexpr bool MULTI = MODE == 1, STATS = MODE == 2, APPLY = MODE == 3, COMPAT = MODE >= 2;
   // exact K codes where scores must be accurate to fp32: fp32 outputs with 8-bit codes (4-bit K scores are
   // accurate enough in the cheap form), and the compat passes, which round every score to the input dtype and must
@@ -234,7 +240,9 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
   const int klane = lane & (LK - 1);                    // K slice: codes [klane*EK, klane*EK + EK)
   const int khalf = lane / LK;                          // which row of a K step
   const int gk = (klane * EK) / p.GS;
-  const int gv = (lane * EV) / p.GS;                    // V slice: codes [lane*EV, lane*EV + EV)
+  // V slice: codes [vlane*EV, vlane*EV + EV) of the rows vrow, vrow + VR, ... of a block (VR = 1 at D >= 256)
+  const int vlane = lane % VL, vrow = lane / VL;
+  const int gv = (vlane * EV) / p.GS;
 
   // the head and rows this lane owns after the reduction
   int my_h = 0;
@@ -507,9 +515,10 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       }
       const float4* psv = reinterpret_cast<const float4*>(sPS) + gv;
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
+      for (int rs = 0; rs < R / VR; ++rs) {
+        const int r = rs * VR + vrow;
         uint32_t w[VW];
-        load_words<VW>(sV + min(r, rows_valid - 1) * W + lane * VW, w);
+        load_words<VW>(sV + min(r, rows_valid - 1) * W + vlane * VW, w);
         float2 f[EV / 2];
         unpack_words<BITS, EXACT, VW>(w, f);
         const float4* pr = psv + r * PS_ROW;
@@ -550,6 +559,17 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
           for (int g = 0; g < NG; ++g) pb[g] += __shfl_xor_sync(0xffffffffu, pb[g], off);
         }
       }
+      if constexpr (!STATS && VR > 1) {
+        // the lanes of one V slice took different rows: add their sums (every lane then holds the slice's total)
+#pragma unroll
+        for (int off = VL; off < 32; off <<= 1)
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+#pragma unroll
+            for (int k = 0; k < EV / 2; ++k)
+              o[h][k] = __fadd2_rn(o[h][k], make_float2(__shfl_xor_sync(0xffffffffu, o[h][k].x, off),
+                                                        __shfl_xor_sync(0xffffffffu, o[h][k].y, off)));
+      }
       if constexpr (!STATS) {
         if (lane < NH) {   // lane < NH owns head my_h; all heads are covered once
 #pragma unroll
@@ -565,11 +585,13 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
       }
       named_barrier_sync(1, NW * 32);   // every warp is done with its scratch before it becomes the combine area
       if constexpr (!STATS) {
+        if (vrow == 0) {
 #pragma unroll
-        for (int h = 0; h < NH; ++h)
+          for (int h = 0; h < NH; ++h)
 #pragma unroll
-          for (int k = 0; k < EV / 2; ++k)
-            reinterpret_cast<float2*>(comb_o + (warp * NH + h) * D + lane * EV)[k] = o[h][k];
+            for (int k = 0; k < EV / 2; ++k)
+              reinterpret_cast<float2*>(comb_o + (warp * NH + h) * D + vlane * EV)[k] = o[h][k];
+        }
       }
       if (lane < NH) {
         comb_m[warp * NH + my_h] = m_run;
@@ -606,31 +628,37 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
   }
 }
 
-template <int BITS, bool EXACT, int MODE, typename Fn>
+// DSET 0: D in {64, 128}; 1: D in {256, 512} (two translation units per (bits, exact), compiled in parallel)
+template <int BITS, bool EXACT, int MODE, int DSET, typename Fn>
 cudaError_t with_split2_kernel_m(int D, int nh, int ng, Fn&& f) {
 #define QDA_V2(D_, NH_, NG_) \
   if (D == D_ && nh == NH_ && ng == NG_) return f(qda_split2_kernel<BITS, D_, NH_, NG_, EXACT, MODE>);
-  QDA_V2(256, 2, 2) QDA_V2(256, 2, 4) QDA_V2(256, 2, 8)
-  QDA_V2(256, 4, 2) QDA_V2(256, 4, 4) QDA_V2(256, 4, 8)
-  QDA_V2(512, 2, 4) QDA_V2(512, 2, 8) QDA_V2(512, 2, 16)
+  if constexpr (DSET == 0) {
+    QDA_V2(64, 2, 1) QDA_V2(64, 2, 2) QDA_V2(64, 4, 1) QDA_V2(64, 4, 2)
+    QDA_V2(128, 2, 1) QDA_V2(128, 2, 2) QDA_V2(128, 2, 4) QDA_V2(128, 4, 1) QDA_V2(128, 4, 2) QDA_V2(128, 4, 4)
+  } else {
+    QDA_V2(256, 2, 2) QDA_V2(256, 2, 4) QDA_V2(256, 2, 8)
+    QDA_V2(256, 4, 2) QDA_V2(256, 4, 4) QDA_V2(256, 4, 8)
+    QDA_V2(512, 2, 4) QDA_V2(512, 2, 8) QDA_V2(512, 2, 16)
+  }
 #undef QDA_V2
   return cudaErrorInvalidValue;
 }
 
-template <int BITS, bool EXACT, typename Fn>
+template <int BITS, bool EXACT, int DSET, typename Fn>
 cudaError_t with_split2_kernel(int D, int nh, int ng, int mode, Fn&& f) {
   switch (mode) {
-    case 0: return with_split2_kernel_m<BITS, EXACT, 0>(D, nh, ng, f);
-    case 1: return with_split2_kernel_m<BITS, EXACT, 1>(D, nh, ng, f);
-    case 2: return with_split2_kernel_m<BITS, false, 2>(D, nh, ng, f);   // pass A reads no V: no exact variant
-    case 3: return with_split2_kernel_m<BITS, EXACT, 3>(D, nh, ng, f);
+    case 0: return with_split2_kernel_m<BITS, EXACT, 0, DSET>(D, nh, ng, f);
+    case 1: return with_split2_kernel_m<BITS, EXACT, 1, DSET>(D, nh, ng, f);
+    case 2: return with_split2_kernel_m<BITS, false, 2, DSET>(D, nh, ng, f);   // pass A reads no V: no exact variant
+    case 3: return with_split2_kernel_m<BITS, EXACT, 3, DSET>(D, nh, ng, f);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <int BITS, bool EXACT>
+template <int BITS, bool EXACT, int DSET>
 cudaError_t launch_split2(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem, cudaStream_t s) {
-  return with_split2_kernel<BITS, EXACT>(D, nh, ng, p.mode, [&](auto kern) -> cudaError_t {
+  return with_split2_kernel<BITS, EXACT, DSET>(D, nh, ng, p.mode, [&](auto kern) -> cudaError_t {
     cudaError_t e = ensure_smem_limit(kern, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, QDA_THREADS, smem, s>>>(p);
@@ -638,10 +666,10 @@ cudaError_t launch_split2(const QdaParams& p, int D, int nh, int ng, dim3 grid, 
   });
 }
 
-template <int BITS, bool EXACT>
+template <int BITS, bool EXACT, int DSET>
 cudaError_t occupancy_split2(int D, int nh, int ng, size_t smem, int* n) {
   // both instances of a shape have the same resources; the single-query one stands for both
-  return with_split2_kernel<BITS, EXACT>(D, nh, ng, 0, [&](auto kern) -> cudaError_t {
+  return with_split2_kernel<BITS, EXACT, DSET>(D, nh, ng, 0, [&](auto kern) -> cudaError_t {
     cudaError_t e = ensure_smem_limit(kern, smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, QDA_THREADS, smem);

@@ -1,11 +1,14 @@
-// Lean split-kernel instantiations for 8-bit codes, 16-bit outputs.
+// Lean split-kernel instantiations for 8-bit codes, 16-bit outputs: D = 256 and 512 here, D = 64 and 128 in
+// qda_split2s_b8_x0.cu.
 #include "qda_split2.cuh"
 
 cudaError_t qda_launch_split2_b8_x0(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem,
                                         cudaStream_t s) {
-  return qda::launch_split2<8, false>(p, D, nh, ng, grid, smem, s);
+  if (D <= 128) return qda_launch_split2s_b8_x0(p, D, nh, ng, grid, smem, s);
+  return qda::launch_split2<8, false, 1>(p, D, nh, ng, grid, smem, s);
 }
 
 cudaError_t qda_occupancy_split2_b8_x0(int D, int nh, int ng, size_t smem, int* n) {
-  return qda::occupancy_split2<8, false>(D, nh, ng, smem, n);
+  if (D <= 128) return qda_occupancy_split2s_b8_x0(D, nh, ng, smem, n);
+  return qda::occupancy_split2<8, false, 1>(D, nh, ng, smem, n);
 }

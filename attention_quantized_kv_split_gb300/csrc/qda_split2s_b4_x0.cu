@@ -1,0 +1,11 @@
+// Lean split-kernel instantiations for 4-bit codes, 16-bit outputs, D = 64 and 128.
+#include "qda_split2.cuh"
+
+cudaError_t qda_launch_split2s_b4_x0(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem,
+                                         cudaStream_t s) {
+  return qda::launch_split2<4, false, 0>(p, D, nh, ng, grid, smem, s);
+}
+
+cudaError_t qda_occupancy_split2s_b4_x0(int D, int nh, int ng, size_t smem, int* n) {
+  return qda::occupancy_split2<4, false, 0>(D, nh, ng, smem, n);
+}

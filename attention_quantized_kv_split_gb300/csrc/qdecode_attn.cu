@@ -111,7 +111,7 @@ Variant pick_variant(int nrep, int D, int GS, int bits) {
   v.W = D * bits / 32;
   v.NG = D / GS;
   const size_t row_bytes = 2 * (size_t)v.W * 4 + 4 * (size_t)v.NG * 2;
-  if (D == 256 || D == 512) {
+  if (D == 64 || D == 128 || D == 256 || D == 512) {
     v.kind = 2;
     v.wpl = v.lpr = v.E = 0;
     v.nh = (nrep <= 2 || D == 512) ? 2 : 4;   // D = 512 takes heads two at a time (register budget)
