@@ -108,13 +108,8 @@ __host__ __device__ inline int split2_scratch_floats(int R, int NG, int NH) {
   return (R * NG * (4 + 2) + R * ((NH / 2) * NG + 1) * 4 + NH * NG + 3) & ~3;
 }
 
-// Launchers of the split kernels, one translation unit per (kernel, bits[, exact]). They return cudaSuccess or the
-// launch error. General kernel: (words per lane, lanes per row, heads per CTA); lean kernel: (D, heads per CTA,
-// groups per row, exact V codes).
-cudaError_t qda_launch_split1_b4(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s);
-cudaError_t qda_launch_split1_b8(const QdaParams& p, int wpl, int lpr, int nh, dim3 grid, size_t smem, cudaStream_t s);
-cudaError_t qda_occupancy_split1_b4(int wpl, int lpr, int nh, size_t smem, int* ctas_per_sm);
-cudaError_t qda_occupancy_split1_b8(int wpl, int lpr, int nh, size_t smem, int* ctas_per_sm);
+// Launchers of the split kernel, translation units per (bits, exact V codes, head-dimension set): (D, heads per CTA,
+// groups per row). They return cudaSuccess or the launch error.
 cudaError_t qda_launch_split2_b4_x0(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem, cudaStream_t s);
 cudaError_t qda_launch_split2_b4_x1(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem, cudaStream_t s);
 cudaError_t qda_launch_split2_b8_x0(const QdaParams& p, int D, int nh, int ng, dim3 grid, size_t smem, cudaStream_t s);

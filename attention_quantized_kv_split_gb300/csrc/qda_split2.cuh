@@ -1,9 +1,9 @@
 // Split kernel, arithmetic-lean variant: D = 64, 128 and 256 with 2 or 4 query heads per CTA, D = 512 with 2
 // (sm_103a).
 //
-// Same data path as qda_split_kernel (one contiguous row range per CTA, producer warp + bulk copies into a
-// shared-memory ring, one partial per (segment, query head)), but the consumer warps are organised around the
-// instruction count per cache row, which bounds this path once the bytes stream at HBM speed:
+// One contiguous row range per CTA, a producer warp streaming it with bulk copies into a shared-memory ring
+// (qda_split.cuh), one partial per (segment, query head); the consumer warps are organised around the instruction
+// count per cache row, which bounds this path once the bytes stream at HBM speed:
 //   * codes become floats with one byte permute each: 4-bit codes as 0.5 + c/256 (K, and V for 16-bit outputs),
 //     8-bit codes as 1 + c/32768 (K for 16-bit outputs), or exactly as c (2^23 + c minus 2^23) where an fp32
 //     output needs it; the constant offset is folded into per-row coefficients A, B with

@@ -11,8 +11,6 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kStages = 4;
-constexpr size_t kStageTarget = 24 * 1024;   // bytes of K+V (codes, scales, biases) per pipeline stage
 constexpr long long kMinRowsPerCta = 128;
 constexpr long long kMaxCtas = 4096;   // the merge kernel stages one weight per partial in shared memory
 
@@ -57,12 +55,6 @@ int cuda_fail(cudaError_t e) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int pow2ceil(int x) {
-  int p = 1;
-  while (p < x) p <<= 1;
-  return p;
-}
-
 // Pure host checks of the shape (no pointers): the support predicate of mlx-bun fused-decode-kernel.ts
 // (fusedDecodeKernelSupported), widened to B >= 1 sequences, any H % Hkv == 0, fp16 or bf16 input and L query
 // positions per sequence.
@@ -94,9 +86,9 @@ int check_dtype(int dtype, int* in, int* out) {
   return QDA_OK;
 }
 
+// The split kernel's configuration for one shape.
 struct Variant {
-  int kind;              // 1: general split kernel, 2: lean kernel for D in {256, 512}
-  int W, wpl, lpr, E, nh, hc, heads_pad, NG, tile, stages;
+  int W, nh, hc, heads_pad, NG, tile, stages;   // words per row, heads per CTA, head chunks, ..., ring stages
   size_t smem;
 };
 
@@ -105,69 +97,42 @@ constexpr size_t kSmemBudget = 112 * 1024;   // two CTAs per SM
 // Rows per warp block of the lean kernel (its Split2Geom<...>::R).
 int split2_rows(int D, int nh) { return nh == 4 ? 8 : 16; }
 
-// nrep: query heads served per KV head (H / Hkv, times L for multi-query decode).
+// nrep: query heads served per KV head (H / Hkv, times L for multi-query decode). D is one of 64, 128, 256, 512.
 Variant pick_variant(int nrep, int D, int GS, int bits) {
   Variant v;
   v.W = D * bits / 32;
   v.NG = D / GS;
-  const size_t row_bytes = 2 * (size_t)v.W * 4 + 4 * (size_t)v.NG * 2;
-  if (D == 64 || D == 128 || D == 256 || D == 512) {
-    v.kind = 2;
-    v.wpl = v.lpr = v.E = 0;
-    v.nh = (nrep <= 2 || D == 512) ? 2 : 4;   // D = 512 takes heads two at a time (register budget)
-    v.hc = (nrep + v.nh - 1) / v.nh;
-    v.heads_pad = v.hc * v.nh;
-    const int R = split2_rows(D, v.nh);
-    v.tile = QDA_SPLIT2_TILE;   // warps take TILE / R blocks of a chunk in turn (the kernel's constant tile)
-    const QdaSmemLayout L = qda_smem_layout(v.tile, 1, v.W, v.NG, v.nh, D);
-    const size_t scratch = (size_t)QDA_NW * split2_scratch_floats(R, v.NG, v.nh) * 4;
-    const size_t comb = (size_t)QDA_NW * v.nh * D * 4 + (size_t)QDA_NW * v.nh * 2 * 4;
-    const size_t tail = std::max(scratch, comb);
-    long long st = ((long long)kSmemBudget - (long long)L.stage0 - (long long)tail) / (long long)L.stage_bytes;
-    v.stages = (int)std::max(2LL, std::min(8LL, st));
-    v.smem = L.stage0 + (size_t)v.stages * L.stage_bytes + tail;
-    return v;
-  }
-  v.kind = 1;
-  v.wpl = v.W > 32 ? v.W / 32 : 1;
-  v.lpr = v.W > 32 ? 32 : v.W;
-  v.E = v.wpl * (32 / bits);
-  const int nh_max = std::min(8, 64 / v.E);
-  v.nh = std::min(pow2ceil(nrep), nh_max);
+  v.nh = (nrep <= 2 || D == 512) ? 2 : 4;   // D = 512 takes heads two at a time (register budget)
   v.hc = (nrep + v.nh - 1) / v.nh;
   v.heads_pad = v.hc * v.nh;
-  int tile = 256;
-  while (tile > 16 && (size_t)tile * row_bytes > kStageTarget) tile >>= 1;
-  v.tile = tile;
-  v.stages = kStages;
-  v.smem = qda_smem_layout(v.tile, v.stages, v.W, v.NG, v.nh, D).total;
+  const int R = split2_rows(D, v.nh);
+  v.tile = QDA_SPLIT2_TILE;   // warps take TILE / R blocks of a chunk in turn (the kernel's constant tile)
+  const QdaSmemLayout L = qda_smem_layout(v.tile, 1, v.W, v.NG, v.nh, D);
+  const size_t scratch = (size_t)QDA_NW * split2_scratch_floats(R, v.NG, v.nh) * 4;
+  const size_t comb = (size_t)QDA_NW * v.nh * D * 4 + (size_t)QDA_NW * v.nh * 2 * 4;
+  const size_t tail = std::max(scratch, comb);
+  long long st = ((long long)kSmemBudget - (long long)L.stage0 - (long long)tail) / (long long)L.stage_bytes;
+  v.stages = (int)std::max(2LL, std::min(8LL, st));
+  v.smem = L.stage0 + (size_t)v.stages * L.stage_bytes + tail;
   return v;
 }
 
 cudaError_t split_occupancy(int bits, int D, bool exact, const Variant& v, int* n) {
-  if (v.kind == 2) {
-    if (bits == 4) {
-      return exact ? qda_occupancy_split2_b4_x1(D, v.nh, v.NG, v.smem, n)
-                   : qda_occupancy_split2_b4_x0(D, v.nh, v.NG, v.smem, n);
-    }
-    return exact ? qda_occupancy_split2_b8_x1(D, v.nh, v.NG, v.smem, n)
-                 : qda_occupancy_split2_b8_x0(D, v.nh, v.NG, v.smem, n);
+  if (bits == 4) {
+    return exact ? qda_occupancy_split2_b4_x1(D, v.nh, v.NG, v.smem, n)
+                 : qda_occupancy_split2_b4_x0(D, v.nh, v.NG, v.smem, n);
   }
-  return bits == 4 ? qda_occupancy_split1_b4(v.wpl, v.lpr, v.nh, v.smem, n)
-                   : qda_occupancy_split1_b8(v.wpl, v.lpr, v.nh, v.smem, n);
+  return exact ? qda_occupancy_split2_b8_x1(D, v.nh, v.NG, v.smem, n)
+               : qda_occupancy_split2_b8_x0(D, v.nh, v.NG, v.smem, n);
 }
 
 cudaError_t split_launch(int bits, bool exact, const QdaParams& p, const Variant& v, dim3 grid, cudaStream_t s) {
-  if (v.kind == 2) {
-    if (bits == 4) {
-      return exact ? qda_launch_split2_b4_x1(p, p.D, v.nh, v.NG, grid, v.smem, s)
-                   : qda_launch_split2_b4_x0(p, p.D, v.nh, v.NG, grid, v.smem, s);
-    }
-    return exact ? qda_launch_split2_b8_x1(p, p.D, v.nh, v.NG, grid, v.smem, s)
-                 : qda_launch_split2_b8_x0(p, p.D, v.nh, v.NG, grid, v.smem, s);
+  if (bits == 4) {
+    return exact ? qda_launch_split2_b4_x1(p, p.D, v.nh, v.NG, grid, v.smem, s)
+                 : qda_launch_split2_b4_x0(p, p.D, v.nh, v.NG, grid, v.smem, s);
   }
-  return bits == 4 ? qda_launch_split1_b4(p, v.wpl, v.lpr, v.nh, grid, v.smem, s)
-                   : qda_launch_split1_b8(p, v.wpl, v.lpr, v.nh, grid, v.smem, s);
+  return exact ? qda_launch_split2_b8_x1(p, p.D, v.nh, v.NG, grid, v.smem, s)
+               : qda_launch_split2_b8_x0(p, p.D, v.nh, v.NG, grid, v.smem, s);
 }
 
 // The plan: one contiguous, equal share of the flattened rows per CTA, as many CTAs as fit on the GPU at once
@@ -223,7 +188,7 @@ DeviceState* device_state(int* dev_out) {
 
 int occupancy_for(DeviceState& d, int bits, int D, bool exact, const Variant& v, int* n) {
   std::lock_guard<std::mutex> lock(d.mu);
-  auto key = std::make_tuple(bits + 16 * (int)exact + 64 * v.kind, D, v.wpl * 64 + v.lpr, v.nh, v.NG, v.smem);
+  auto key = std::make_tuple(bits + 16 * (int)exact, D, 0, v.nh, v.NG, v.smem);
   auto it = d.occupancy.find(key);
   if (it != d.occupancy.end()) {
     *n = it->second;

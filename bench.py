@@ -334,7 +334,7 @@ def run_ours(args):
     achieved = nbytes / (split_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
-                "kernel": "qda_split2_kernel" if w.D in (256, 512) else "qda_split_kernel", "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                "kernel": "qda_split2_kernel", "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6800 GB/s",
                 "split_kernel_us": round(split_ms * 1e3, 3), "merge_kernel_us": round(merge_ms * 1e3, 3),
                 "algorithmic_bytes_per_launch": nbytes}

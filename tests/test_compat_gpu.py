@@ -149,8 +149,8 @@ def test_compat_differs_from_exact_softmax_where_rounding_matters():
 
 
 @pytest.mark.parametrize("D", [64, 128])
-def test_compat_general_kernel_gqa_and_splits(D):
-    # D = 64 and 128 run on the general split kernel
+def test_compat_small_head_dims_gqa_and_splits(D):
+    # D = 64 and 128: 8 or 4 K lanes per row, V rows shared by 8 or 16 lanes
     check(synth.small(B=2, H=24, Hkv=3, D=D, N=(900, 50), bits=8, GS=32, seed=D))
     check(synth.small(B=2, H=8, Hkv=2, D=D, N=(300, 77), bits=4, GS=32, dtype_in="fp16", seed=D + 1), "fp32",
           splits=37)
