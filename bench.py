@@ -13,6 +13,7 @@ Prints one JSON line. Under torchrun (N > 1) every rank runs an independent repl
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -365,10 +366,14 @@ def run_ours(args):
 
     extra = {}
     if not args.no_extra:
-        for idx in (3, 4, 5):
+        # workloads 3-5, then a head dimension of 128 (the most common one in deployed models) on the shape of the
+        # 32k workload: B1 H32 Hkv8 D128 N32768, 4-bit, GS 64 (the same 37.7 MB of cache as the 8k workload)
+        d128 = dataclasses.replace(synth.small(B=1, H=32, Hkv=8, D=128, N=(32768,), bits=4, GS=64, seed=20261202 + 128),
+                                   name="d128_B1_H32_Hkv8_D128_N32768_4b_GS64_bf16")
+        for idx in (3, 4, 5, d128):
             if idx == args.workload:
                 continue
-            wx = synth.workload(idx)
+            wx = synth.workload(idx) if isinstance(idx, int) else idx
             Nx, qx, cx = make_workload(wx, device)
             ox = torch.empty((wx.B, wx.H, wx.D), dtype=synth.DT[wx.dtype_out], device=device)
             fx = qda.bind_decode_attention(qx, cx, ox, stream)
@@ -382,17 +387,16 @@ def run_ours(args):
             del cx, qx, ox
             torch.cuda.empty_cache()
         # the two-pass compat form on this workload's cache (K read in both passes)
-        if w.D in (256, 512):
-            oc = torch.empty_like(out)
-            ccall = lambda: qda.qdecode_attn_compat(q, cache.kp, cache.ks, cache.kb, cache.vp, cache.vs, cache.vb, oc,
-                                                    N, w.Hkv, w.GS, w.bits, stream)
-            for _ in range(5):
-                ccall()
-            mc = statistics.mean(time_calls(ccall, 50, flush, stream))
-            extra[f"{w.name}_two_pass_compat"] = {
-                "us_per_call": round(mc * 1e3, 2), "kv_GBps": round(nbytes / (mc * 1e-3) / 1e9, 1),
-                "frac_of_peak": round(nbytes / (mc * 1e-3) / 1e9 / peak, 4), "kv_bytes": nbytes,
-                "note": "K is read in both passes; kv_GBps counts each KV byte once"}
+        oc = torch.empty_like(out)
+        ccall = lambda: qda.qdecode_attn_compat(q, cache.kp, cache.ks, cache.kb, cache.vp, cache.vs, cache.vb, oc,
+                                                N, w.Hkv, w.GS, w.bits, stream)
+        for _ in range(5):
+            ccall()
+        mc = statistics.mean(time_calls(ccall, 50, flush, stream))
+        extra[f"{w.name}_two_pass_compat"] = {
+            "us_per_call": round(mc * 1e3, 2), "kv_GBps": round(nbytes / (mc * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(nbytes / (mc * 1e-3) / 1e9 / peak, 4), "kv_bytes": nbytes,
+            "note": "K is read in both passes; kv_GBps counts each KV byte once"}
         # the codec under a plain GEMV: an MLP-sized 8-bit matrix (K = 4096, N = 14336, GS = 64) times one vector;
         # random codes, scales and biases (the kernel's time does not depend on their values)
         gK, gN, gGS = 4096, 14336, 64
