@@ -27,6 +27,7 @@ struct QdaParams {
   long long total_rows;       // T = Hkv * sum(N)
   unsigned long long cta_magic;   // ceil(2^64 / num_ctas): qda_cta_row_fast divides by num_ctas with it
   int B, H, Hkv, D, GS, NG, W, nrep, heads_pad, head_chunks, num_ctas, tile_rows, stages;
+  int kstages;                // tensor-core kernel: depth of the K-code ring (stages: of the V ring)
   int L;                      // query positions per sequence; head j of a KV head is (position j / nrep, j % nrep)
   int mode;                   // lean split kernel: 0 single-pass, 1 multi-query, 2 compat pass A, 3 compat pass B
   int k_only;                 // the ring carries K only (compat pass A)
@@ -107,6 +108,70 @@ __host__ __device__ inline QdaSmemLayout qda_smem_layout(int tile_rows, int stag
 __host__ __device__ inline int split2_scratch_floats(int R, int NG, int NH) {
   return (R * NG * (4 + 2) + R * ((NH / 2) * NG + 1) * 4 + NH * NG + 3) & ~3;
 }
+
+// ---------------------------------------------------------------------- tensor-core split kernel (4-bit codes)
+// Warp roles of the tensor-core split kernel (one CTA per SM): converters turn a tile's K codes into the MMA's A
+// operand in tensor memory, epilogue warps turn the MMA's sums into scores and weights, V warps accumulate the V
+// rows on the CUDA cores; one producer warp streams the cache, two warps issue the MMAs.
+#define QDA_TC_CONV 4
+#define QDA_TC_EPI 4
+#define QDA_TC_VW 8
+#define QDA_TC_WARPS (QDA_TC_CONV + QDA_TC_EPI + QDA_TC_VW + 3)
+#define QDA_TC_THREADS (QDA_TC_WARPS * 32)
+#define QDA_TC_TILE 128   // rows per pipeline tile: the M of every MMA
+
+// Shared-memory layout of the tensor-core split kernel for one (D, heads per CTA, groups per row) and ring depths:
+// a ring of K-code tiles (kept until converted) and a ring of V-code + scale/bias tiles (kept until the scores and
+// the V rows are done).
+struct QdaTcLayout {
+  size_t b_op;         // [2] B operand: q of a unit's heads, 16 x D 16-bit values in K-major core matrices
+  size_t qs;           // [2][NG][NH] fp32 sums of q per group
+  size_t alpha;        // [2][4][NH] fp32 rescale factors per tile, lane quarter and head
+  size_t ps;           // [2][128][ps_row] float4: p * A_v per (row, group), four heads; also the combine area
+  int ps_row;          // float4 per row of ps (NG, plus one against bank conflicts)
+  size_t k_bytes;      // one K tile (tile rows x D / 2 bytes, 16-byte chunks swizzled by the tensor copy)
+  size_t v_bytes;      // V codes of one tile
+  size_t sc_bytes;     // one scale or bias array of a tile (tile rows x NG 16-bit values, 16-byte multiple)
+  size_t vstage_bytes; // V codes, K scales, K biases, V scales, V biases
+  size_t k0, v0;       // offsets of the K ring (1024-byte aligned: the swizzle follows address bits 4..9) and V ring
+  size_t total;
+};
+
+// Bytes the segment-end combine needs: every V warp's o[NH][D], per lane quarter the (max, sum) per head and the
+// p * B_v sums per (group, head).
+__host__ __device__ inline size_t qda_tc_combine_bytes(int D, int NH, int NG) {
+  return (size_t)QDA_TC_VW * NH * D * 4 + 4 * (size_t)NH * 2 * 4 + 4 * (size_t)NG * NH * 4;
+}
+
+__host__ __device__ inline QdaTcLayout qda_tc_layout(int D, int NH, int NG, int kstages, int vstages) {
+  QdaTcLayout L;
+  const size_t RB = (size_t)D / 2;
+  L.b_op = 1024;   // barriers, the abort word and the tensor-memory address sit below
+  L.qs = L.b_op + 2 * 32 * (size_t)D;
+  L.alpha = L.qs + 2 * (size_t)NG * NH * 4;
+  L.ps = (L.alpha + 2 * 4 * (size_t)NH * 4 + 15) & ~(size_t)15;
+  L.ps_row = NG + 1;
+  size_t ps_bytes = 2 * (size_t)QDA_TC_TILE * L.ps_row * 16;
+  const size_t cb = qda_tc_combine_bytes(D, NH, NG);
+  if (cb > ps_bytes) ps_bytes = cb;
+  L.k_bytes = (size_t)QDA_TC_TILE * RB;
+  L.v_bytes = (size_t)QDA_TC_TILE * RB;
+  L.sc_bytes = ((size_t)QDA_TC_TILE * NG * 2 + 15) & ~(size_t)15;
+  L.vstage_bytes = L.v_bytes + 4 * L.sc_bytes;
+  L.k0 = (L.ps + ps_bytes + 1023) & ~(size_t)1023;
+  L.v0 = L.k0 + (size_t)kstages * L.k_bytes;
+  L.total = L.v0 + (size_t)vstages * L.vstage_bytes;
+  return L;
+}
+
+// Tensor-core split kernel launches (tmap_k: the CUtensorMap of the K codes, a second kernel parameter) and their
+// occupancy, per V-code form (x1: exact codes for fp32 outputs); D in {128, 256}, nh = 4, ng = D / GS >= 2.
+cudaError_t qda_launch_tc_x0(const QdaParams& p, const void* tmap_k, int D, int nh, int ng, dim3 grid, size_t smem,
+                             cudaStream_t s);
+cudaError_t qda_launch_tc_x1(const QdaParams& p, const void* tmap_k, int D, int nh, int ng, dim3 grid, size_t smem,
+                             cudaStream_t s);
+cudaError_t qda_occupancy_tc_x0(int D, int nh, int ng, size_t smem, int* ctas_per_sm);
+cudaError_t qda_occupancy_tc_x1(int D, int nh, int ng, size_t smem, int* ctas_per_sm);
 
 // Launchers of the split kernel, translation units per (bits, exact V codes, head-dimension set): (D, heads per CTA,
 // groups per row). They return cudaSuccess or the launch error.

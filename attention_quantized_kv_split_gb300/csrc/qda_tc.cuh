@@ -1,0 +1,622 @@
+// Tensor-core split kernel of quantized-KV decode attention for 4-bit codes (sm_103a): the q . K contraction of
+// every 128-row tile runs on tcgen05 with the codes as exact 16-bit operands; the softmax and the V side stay on
+// the CUDA cores in fp32.
+//
+// The block structure is the flash-decoding split-N of mlx-bun fused-decode-kernel.ts (BLOCK_SOURCE: per-block
+// running max / sum-exp / unnormalised o, merged later by MERGE_SOURCE) over one contiguous row range per CTA
+// (qda_split.cuh). What is new is where the score dot product runs. With four query heads per KV head and 4-bit
+// codes, a CUDA-core kernel spends most of its issue slots on the scores (unpacking, 4 x D FMAs, a cross-lane
+// reduction); here a row's codes are turned into sixteen-bit values and the tensor cores do the sums:
+//   * a 4-bit code c becomes the bf16 (or fp16) value 128 + c (1024 + c): one AND/OR per two codes, exact;
+//   * the factored dot of the SCORE_ROW comment, s * sum_g(c q) + b * sum_g(q), is taken per group g of GS
+//     codes: one MMA chain per group writes sum_{d in g} (OFF + c_d) q_d for the CTA's four heads into its own
+//     16 accumulator columns (M = 128 rows, N = 16 with heads 4..15 zero, K = 16 per instruction, fp32 sums),
+//     and the epilogue forms s * acc + (b - OFF * s) * sum_g(q) in fp32;
+//   * the A operand (the codes) goes from the registers straight into tensor memory, the B operand (q of the
+//     unit, its own 16-bit values, exact) sits in shared memory.
+// One thread issues a tcgen05 MMA about every 50 cycles whatever its N up to 128, so a tile's D / 16 MMAs take a
+// fixed time to issue; two issuing warps halve it, and every stage of a tile runs in its own warps, linked by
+// mbarriers, so that tile i + 1 is converted and multiplied while tile i's scores and tile i - 1's V rows are
+// worked on:
+//   warps 0-3   converters: K codes of a tile (lane quarter w: rows 32 w .. 32 w + 31) -> tensor memory (A), and at
+//               a new (sequence, KV head) the unit's q into the B operand and its per-group sums;
+//   warps 4-7   epilogue: accumulators of their lane quarter -> scores, the online softmax (reference max per
+//               quarter and head), p * A_v per (row, group) for the V warps, sums of p and of p * B_v;
+//   warps 8-15  V: 16 rows each of every tile, all four heads, packed fp32 FMAs on the CUDA cores;
+//   warp 16     producer: 2-D tensor copies of the K tiles (their 128-byte swizzle lets one thread per row read its
+//               row without bank conflicts) into one ring, 1-D bulk copies of the V codes, scales and biases into
+//               a second;
+//   warps 17-18 issue the MMAs of even and odd tiles (double-buffered A operand and accumulators in tensor
+//               memory, which warp 17 allocates and frees).
+// Every wait is bounded; after a timeout every warp still passes every barrier (with no work), so the kernel
+// always returns and frees its tensor memory.
+#pragma once
+
+#include <cuda.h>
+
+#include "qda_split2.cuh"
+
+namespace qda {
+
+__host__ __device__ constexpr int tc_tmem_cols(int used) {
+  return used <= 32 ? 32 : used <= 64 ? 64 : used <= 128 ? 128 : used <= 256 ? 256 : 512;
+}
+
+// Bounded wait on a barrier phase taken by lane 0, its result shared with the warp (warp-uniform control flow).
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned int* err) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, abort, err, 1u);
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// The V codes of chunk [c0, c1) of the tile starting at row t0 and the 8-row aligned cover of its scales and biases
+// into V-ring slot `vst`, completing on `full`. Called by the producer warp.
+__device__ __forceinline__ void tc_issue_v(const QdaParams& p, unsigned char* vst, const QdaTcLayout& L,
+                                           uint64_t* full, long long c0, long long c1, long long t0, long long T,
+                                           uint64_t pol) {
+  const int lane = threadIdx.x & 31;
+  const int NG = p.NG;
+  const uint32_t RB = p.W * 4, SB = NG * 2;
+  const uint32_t cbytes = (uint32_t)(c1 - c0) * RB;
+  const size_t coff = (size_t)(c0 - t0) * RB;
+  const long long s0 = c0 & ~7LL;
+  const long long s1 = min((c1 + 7) & ~7LL, T);
+  const uint32_t sbytes = (uint32_t)(s1 - s0) * SB;
+  const uint32_t s16 = sbytes & ~15u;
+  const size_t soff = (size_t)(s0 - t0) * SB;
+  unsigned char* sc = vst + L.v_bytes;
+  const bool inb = in_bounds(c0 >= t0 && c0 < c1 && c1 <= T && c1 - t0 <= QDA_TC_TILE && s1 <= T && s0 >= t0 &&
+                                 coff + cbytes <= L.v_bytes && soff + sbytes <= L.sc_bytes,
+                             p.err);
+  if (lane == 0 && !inb) mbar_arrive_expect_tx(full, 0);
+  if (!inb) return;
+  if (lane == 0) {
+    if (s16 != sbytes) {   // a ragged last < 16 bytes of the scale arrays: plain loads, published by the arrive
+      const uint16_t* srcs[4] = {p.ks, p.kb, p.vs, p.vb};
+      for (int a = 0; a < 4; ++a) {
+        const uint16_t* src = srcs[a] + s0 * NG + s16 / 2;
+        uint16_t* dst = reinterpret_cast<uint16_t*>(sc + a * L.sc_bytes + soff + s16);
+        for (uint32_t k = 0; k < (sbytes - s16) / 2; ++k) dst[k] = src[k];
+      }
+    }
+    mbar_arrive_expect_tx(full, cbytes + 4 * s16);
+  }
+  __syncwarp();
+  if (lane == 0) {
+    bulk_g2s(vst + coff, p.vp + c0 * p.W, cbytes, full, pol);
+  } else if (lane < 5 && s16) {
+    const int a = lane - 1;
+    const uint16_t* src = a == 0 ? p.ks : a == 1 ? p.kb : a == 2 ? p.vs : p.vb;
+    bulk_g2s(sc + a * L.sc_bytes + soff, src + s0 * NG, s16, full, pol);
+  }
+}
+
+template <int D, int NH, int NG, bool EXACT>
+__global__ void __launch_bounds__(QDA_TC_THREADS, 1)
+    qda_tc_kernel(const __grid_constant__ QdaParams p, const __grid_constant__ CUtensorMap tmk) {
+  constexpr int TILE = QDA_TC_TILE;
+  constexpr int RB = D / 2, W = D / 8, CPR = RB / 16, GS = D / NG;
+  constexpr int EV = D >= 256 ? D / 32 : 8, VL = D / EV, VR = 32 / VL, VW = EV / 8;
+  constexpr int A_COLS = D / 2, ACC_COLS = 16 * NG;
+  constexpr int TMEM_COLS = tc_tmem_cols(2 * A_COLS + 2 * ACC_COLS);
+  constexpr int KSTEPS = D / 16;
+  constexpr int REGIONS = RB >= 128 ? RB / 128 : 1;
+  constexpr int EPI0 = QDA_TC_CONV, V0 = EPI0 + QDA_TC_EPI, PRODUCER = V0 + QDA_TC_VW, MMA_WARP = PRODUCER + 1;
+  // MMA_WARP issues the MMAs of even tiles and allocates tensor memory, MMA_WARP + 1 those of odd tiles
+  constexpr int EV_THREADS = (QDA_TC_EPI + QDA_TC_VW) * 32;
+  static_assert(NH == 4, "four query heads per CTA");
+  static_assert(NG >= 2 && GS >= 32 && GS % 16 == 0, "two or more groups of at least 32 codes per row");
+  static_assert(2 * A_COLS + 2 * ACC_COLS <= 512, "tensor memory");
+  static_assert(RB == 64 || RB % 128 == 0, "K rows of 64 or 128k bytes");
+  static_assert(QDA_TC_VW * 16 == TILE && QDA_TC_CONV * 32 == TILE && QDA_TC_EPI * 32 == TILE, "warp shares");
+
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int KS = p.kstages, VS = p.stages;
+  const QdaTcLayout Ls = qda_tc_layout(D, NH, NG, KS, VS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* kfull = bars;          // [KS <= 8] K tile landed
+  uint64_t* kempty = bars + 8;     // [KS] K tile converted (4 converter warps)
+  uint64_t* vfull = bars + 16;     // [VS <= 12] V codes and scales landed
+  uint64_t* vempty = bars + 28;    // [VS] scales and V rows used (4 epilogue + 8 V warps)
+  uint64_t* a_full = bars + 40;    // [2] A buffer written (4 converter warps)
+  uint64_t* a_free = bars + 42;    // [2] the MMAs that read A buffer b are complete
+  uint64_t* acc_full = bars + 44;  // [2] accumulator buffer b holds the tile's sums
+  uint64_t* acc_empty = bars + 46; // [2] accumulator buffer b read (4 epilogue warps)
+  uint64_t* p_full = bars + 48;    // [2] p * A_v buffer b written (4 epilogue warps)
+  uint64_t* p_empty = bars + 50;   // [2] p * A_v buffer b read (8 V warps)
+  uint64_t* qs_full = bars + 52;   // [2] B operand and q sums of unit parity b written (4 converter warps)
+  uint64_t* qs_free = bars + 54;   // [2] q sums of unit parity b no longer read (4 epilogue warps)
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 480);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 484);
+  unsigned char* b_op = smem + Ls.b_op;
+  float* qs_all = reinterpret_cast<float*>(smem + Ls.qs);
+  float* alpha_s = reinterpret_cast<float*>(smem + Ls.alpha);
+  float4* ps = reinterpret_cast<float4*>(smem + Ls.ps);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta = blockIdx.x / p.head_chunks, hc = blockIdx.x - cta * p.head_chunks;
+  const long long T = p.total_rows;
+  const long long r0 = qda_cta_row_fast(T, p.num_ctas, p.cta_magic, cta);
+  const long long r1 = qda_cta_row_fast(T, p.num_ctas, p.cta_magic, cta + 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], QDA_TC_CONV);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], QDA_TC_EPI + QDA_TC_VW);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&a_full[k], QDA_TC_CONV);
+      mbar_init(&a_free[k], 1);
+      mbar_init(&acc_full[k], 1);
+      mbar_init(&acc_empty[k], QDA_TC_EPI);
+      mbar_init(&p_full[k], QDA_TC_EPI);
+      mbar_init(&p_empty[k], QDA_TC_VW);
+      mbar_init(&qs_full[k], QDA_TC_CONV);
+      mbar_init(&qs_free[k], QDA_TC_EPI);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == MMA_WARP) tmem_alloc(tmem_slot, TMEM_COLS);
+  // B operand rows (heads) 4..15 of both buffers stay zero for the whole kernel
+  for (int k = threadIdx.x; k < 4 * D; k += QDA_TC_THREADS) reinterpret_cast<uint4*>(b_op)[k] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  pdl_launch_dependents();
+
+  if (r0 < r1) {
+    ChunkWalker walk;
+    walk.init(p, r0, r1);
+    long long c0, c1, t0;
+    const bool f16 = p.f16 != 0;
+
+    if (warp == PRODUCER) {
+      // ---------------------------------------------------------------------------------- producer warp
+      const uint64_t pol = policy_evict_first();
+      int i = 0, ks = 0, kph = 0, vs = 0, vph = 0;
+      while (walk.next(p, c0, c1, t0)) {
+        if (blockIdx.x == 0 && i == p.stall_chunk) break;   // testing aid: the consumers' wait for it must run out
+        if (i >= KS && !wait_warp(&kempty[ks], kph ^ 1, abort_flag, p.err)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&kfull[ks], (uint32_t)Ls.k_bytes);
+          unsigned char* kst = smem + Ls.k0 + (size_t)ks * Ls.k_bytes;
+          for (int rg = 0; rg < REGIONS; ++rg)   // the whole tile: rows past the cache read as zero
+            tma_load_2d(kst + (size_t)rg * TILE * 128, &tmk, rg * 128, (int)t0, &kfull[ks], pol);
+        }
+        __syncwarp();
+        if (i >= VS && !wait_warp(&vempty[vs], vph ^ 1, abort_flag, p.err)) break;
+        tc_issue_v(p, smem + Ls.v0 + (size_t)vs * Ls.vstage_bytes, Ls, &vfull[vs], c0, c1, t0, T, pol);
+        ++i;
+        if (++ks == KS) {
+          ks = 0;
+          kph ^= 1;
+        }
+        if (++vs == VS) {
+          vs = 0;
+          vph ^= 1;
+        }
+      }
+      if (lane == 0) {   // every issued copy lands before the CTA exits
+        for (int j = (i > KS ? i - KS : 0); j < i; ++j) mbar_wait_drain(&kfull[j % KS], (j / KS) & 1, p.err);
+        for (int j = (i > VS ? i - VS : 0); j < i; ++j) mbar_wait_drain(&vfull[j % VS], (j / VS) & 1, p.err);
+      }
+      __syncwarp();
+    } else if (warp >= MMA_WARP) {
+      // ---------------------------------------------------------------------------------- MMA warps
+      // Two issuers, one per A / accumulator buffer (tile parity): one thread issues an MMA about every 50
+      // cycles, and two threads keep the tensor pipe twice as busy.
+      const int ab = warp - MMA_WARP;
+      const uint32_t idesc = mma_idesc_f16(TILE, 16, f16);
+      // descriptor of K step 0 of B buffer 0; step s of buffer u adds (u * 32 D + 512 s) / 16 to the address field
+      const uint64_t bdesc0 = smem_desc_kmajor(smem_addr(b_op), 256, 128);
+      const uint32_t a0 = tbase + ab * A_COLS;
+      const uint32_t d0 = tbase + 2 * A_COLS + ab * ACC_COLS;
+      int i = 0, uidx = -1, cur_unit = -1, issued = -1;
+      while (walk.next(p, c0, c1, t0)) {
+        if (walk.unit != cur_unit) {
+          cur_unit = walk.unit;
+          ++uidx;
+        }
+        if ((i & 1) == ab) {
+          if (!wait_warp(&a_full[ab], (i >> 1) & 1, abort_flag, p.err)) break;
+          if (i >= 2 && !wait_warp(&acc_empty[ab], ((i >> 1) - 1) & 1, abort_flag, p.err)) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint64_t bd = bdesc0 + (uint64_t)((uidx & 1) * 2 * D);
+#pragma unroll
+            for (int s = 0; s < KSTEPS; ++s) {
+              // K step s covers codes of group (16 s) / GS; the group's first step starts its accumulator afresh
+              mma_f16_ts(d0 + 16 * ((16 * s) / GS), a0 + 8 * s, bd + (uint64_t)(32 * s), idesc, (16 * s) % GS != 0);
+            }
+            mma_commit(&a_free[ab]);
+            mma_commit(&acc_full[ab]);
+          }
+          __syncwarp();
+          issued = i;
+        }
+        ++i;
+      }
+      // every MMA this warp issued is complete before the tensor memory is freed
+      if (issued >= 0 && lane == 0) mbar_wait_drain(&a_free[ab], (issued >> 1) & 1, p.err);
+      __syncwarp();
+    } else if (warp < EPI0) {
+      // ---------------------------------------------------------------------------------- converter warps
+      const int m = 32 * warp + lane;   // the tile row this thread converts
+      const uint32_t tl = tbase + ((uint32_t)(32 * warp) << 16);
+      const uint32_t magic = f16 ? 0x64006400u : 0x43004300u;   // OFF + c in the low mantissa bits
+      int i = 0, ks = 0, kph = 0, uidx = -1, cur_unit = -1;
+      bool ok = true;   // false once a wait of this warp gave up: the warp then passes every barrier with no work
+      while (walk.next(p, c0, c1, t0)) {
+        ok = ok && wait_warp(&kfull[ks], kph, abort_flag, p.err);
+        // A buffer i & 1 was last read by the MMAs of tile i - 2
+        if (i >= 2) ok = ok && wait_warp(&a_free[i & 1], ((i >> 1) - 1) & 1, abort_flag, p.err);
+        tc_fence_after();
+        if (walk.unit != cur_unit) {
+          // a new (sequence, KV head): its q into B operand buffer (unit parity) and its sums per group, once the
+          // epilogue is done with the unit two back (the MMAs that read that buffer are complete: tile i - 2)
+          cur_unit = walk.unit;
+          ++uidx;
+          const int par = uidx & 1;
+          if (uidx >= 2) ok = ok && wait_warp(&qs_free[par], ((uidx >> 1) - 1) & 1, abort_flag, p.err);
+          if (ok) {
+            constexpr int OCT = D / 8;
+            const int item = threadIdx.x;   // (head, octet of q): converter threads 0..127
+            float sum = 0.f;
+            if (item < NH * OCT) {
+              const int h = item / OCT, wi = item - h * OCT;
+              const int j = hc * NH + h;
+              uint4 a = make_uint4(0, 0, 0, 0);
+              if (j < p.nrep * p.L) {
+                const long long row = qda_q_row(walk.b, walk.kvh, j, p.nrep, p.L, p.H);
+                if (in_bounds(row < (long long)p.B * p.L * p.H, p.err))
+                  a = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) + row * D + 8 * wi);
+              }
+              // position 2j + e of octet wi holds q[8 wi + j + 4 e]: the order in which the conversion below lays
+              // the codes of a word into tensor-memory columns
+              const uint4 bw = make_uint4(__byte_perm(a.x, a.z, 0x5410), __byte_perm(a.x, a.z, 0x7632),
+                                          __byte_perm(a.y, a.w, 0x5410), __byte_perm(a.y, a.w, 0x7632));
+              *reinterpret_cast<uint4*>(b_op + par * 32 * D + wi * 256 + (h >> 3) * 128 + (h & 7) * 16) = bw;
+              const uint32_t u[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                sum += half_bits_to_float_rt(u[k] & 0xFFFFu, f16) + half_bits_to_float_rt(u[k] >> 16, f16);
+            }
+#pragma unroll
+            for (int off = 1; off < GS / 8; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            if (item < NH * OCT) {
+              const int h = item / OCT, wi = item - h * OCT;
+              if ((wi & (GS / 8 - 1)) == 0) qs_all[par * NG * NH + (wi / (GS / 8)) * NH + h] = sum;
+            }
+          }
+          fence_proxy_async();
+          named_barrier_sync(2, QDA_TC_CONV * 32);
+          if (lane == 0) mbar_arrive(&qs_full[par]);
+        }
+        if (ok) {
+          const unsigned char* sK = smem + Ls.k0 + (size_t)ks * Ls.k_bytes;
+#pragma unroll 2
+          for (int c = 0; c < CPR; ++c) {
+            const unsigned char* src;
+            if constexpr (RB == 64) {
+              src = sK + m * 64 + ((c ^ ((m >> 1) & 3)) << 4);
+            } else {
+              src = sK + (c >> 3) * (TILE * 128) + m * 128 + (((c & 7) ^ (m & 7)) << 4);
+            }
+            const uint4 x = *reinterpret_cast<const uint4*>(src);
+            const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+            uint32_t out[16];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              // column 4 w + j of word w holds (code j, code j + 4) of the word as (low, high) halves
+              out[4 * t + 0] = (wv[t] & 0x000F000Fu) | magic;
+              out[4 * t + 1] = ((wv[t] >> 4) & 0x000F000Fu) | magic;
+              out[4 * t + 2] = ((wv[t] >> 8) & 0x000F000Fu) | magic;
+              out[4 * t + 3] = ((wv[t] >> 12) & 0x000F000Fu) | magic;
+            }
+            tmem_st16(tl + (i & 1) * A_COLS + 16 * c, out);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&kempty[ks]);
+          mbar_arrive(&a_full[i & 1]);
+        }
+        ++i;
+        if (++ks == KS) {
+          ks = 0;
+          kph ^= 1;
+        }
+      }
+    } else {
+      // ---------------------------------------------------------------------------- epilogue and V warps
+      const bool epi = warp < V0;
+      const int q = epi ? warp - EPI0 : (warp - V0) >> 1;   // lane quarter (rows 32 q .. 32 q + 31)
+      const int ev_tid = threadIdx.x - EPI0 * 32;
+      float* co = reinterpret_cast<float*>(smem + Ls.ps);   // segment-end combine area (the p * A_v buffers)
+      float* cm = co + QDA_TC_VW * NH * D;
+      float* cl = cm + 4 * NH;
+      float* cpb = cl + 4 * NH;
+      // End of a segment, after both roles wrote their parts: one partial (max, sum, o[D]) per head from the four
+      // lane quarters, combined in a fixed order by the 384 epilogue and V threads. The area is free: the V warps
+      // are past this tile and the epilogue warps have not started the next.
+      auto combine = [&](int unit) {
+        named_barrier_sync(1, EV_THREADS);
+        const long long slot = (long long)cta + unit;
+        for (int idx = ev_tid; idx < NH * D; idx += EV_THREADS) {
+          const int h = idx / D, d = idx - h * D, g = d / GS;
+          float M = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) M = fmaxf(M, cm[k * NH + h]);
+          float O = 0.f, Lsum = 0.f;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float mk = cm[k * NH + h];
+            const float wt = mk == -INFINITY ? 0.f : ex2(mk - M);
+            const float ok4 = co[(2 * k * NH + h) * D + d] + co[((2 * k + 1) * NH + h) * D + d] +
+                              cpb[(k * NG + g) * NH + h];
+            O = fmaf(wt, ok4, O);
+            Lsum = fmaf(wt, cl[k * NH + h], Lsum);
+          }
+          const size_t hp = (size_t)slot * p.heads_pad + (size_t)hc * NH + h;
+          if (!in_bounds(slot < (long long)p.num_ctas + p.B * p.Hkv && hc * NH + h < p.heads_pad, p.err)) continue;
+          p.part_o[hp * D + d] = O;
+          if (d == 0) p.part_ml[hp] = make_float2(M, Lsum);
+        }
+        named_barrier_sync(1, EV_THREADS);
+      };
+      int i = 0, vs = 0, vph = 0;
+      bool ok = true;   // false once a wait of this warp gave up: the warp then passes every barrier with no work
+
+      if (epi) {
+        // ------------------------------------------------------------------------------ epilogue warps
+        const int m = 32 * q + lane;   // the row this thread scores
+        const uint32_t tl = tbase + ((uint32_t)(32 * q) << 16);
+        const float OFF = f16 ? 1024.f : 128.f;
+        // reference max, sum of weights and sums of p * B_v over this thread's rows, per head
+        float m_run[NH], l_run[NH];
+        float pb[NG][NH];
+        auto reset = [&]() {
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            m_run[h] = -INFINITY;
+            l_run[h] = 0.f;
+#pragma unroll
+            for (int g = 0; g < NG; ++g) pb[g][h] = 0.f;
+          }
+        };
+        reset();
+        int uidx = -1, cur_unit = -1;
+        while (walk.next(p, c0, c1, t0)) {
+          const unsigned char* vst = smem + Ls.v0 + (size_t)vs * Ls.vstage_bytes;
+          const int lr0 = (int)(c0 - t0), lr1 = (int)(c1 - t0);
+          const int pbuf = i & 1;
+          if (walk.unit != cur_unit) {
+            cur_unit = walk.unit;
+            ++uidx;
+            ok = ok && wait_warp(&qs_full[uidx & 1], (uidx >> 1) & 1, abort_flag, p.err);
+          }
+          const float* qs = qs_all + (uidx & 1) * NG * NH;
+          ok = ok && wait_warp(&acc_full[pbuf], (i >> 1) & 1, abort_flag, p.err);
+          tc_fence_after();
+          float acc[NG][NH];
+          if (ok) {
+#pragma unroll
+            for (int g = 0; g < NG; ++g) tmem_ld<NH>(tl + 2 * A_COLS + pbuf * ACC_COLS + 16 * g, acc[g]);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int g = 0; g < NG; ++g)
+#pragma unroll
+              for (int h = 0; h < NH; ++h) acc[g][h] = 0.f;
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[pbuf]);
+          ok = ok && wait_warp(&vfull[vs], vph, abort_flag, p.err);
+          const uint16_t* sKS = reinterpret_cast<const uint16_t*>(vst + Ls.v_bytes);
+          const uint16_t* sKB = sKS + Ls.sc_bytes / 2;
+          const uint16_t* sVS = sKB + Ls.sc_bytes / 2;
+          const uint16_t* sVB = sVS + Ls.sc_bytes / 2;
+          const bool valid = m >= lr0 && m < lr1;
+          float sc[NH];
+#pragma unroll
+          for (int h = 0; h < NH; ++h) sc[h] = 0.f;
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            const float s = half_bits_to_float_rt(sKS[m * NG + g], f16);
+            const float b = half_bits_to_float_rt(sKB[m * NG + g], f16);
+            const float S = p.qscale * s;
+            const float Bc = p.qscale * fmaf(-OFF, s, b);
+            const float4 q4 = reinterpret_cast<const float4*>(qs)[g];
+            const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+            for (int h = 0; h < NH; ++h) sc[h] = fmaf(S, acc[g][h], fmaf(Bc, qv[h], sc[h]));
+          }
+          bool need = false;
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            if (!valid) sc[h] = -INFINITY;
+            need |= sc[h] > m_run[h] + 8.f;
+          }
+          // lazy rescaling: the reference max of a head moves only when a score passes it by more than 8 (a
+          // factor 2^8 in the weights)
+          float alpha[NH];
+#pragma unroll
+          for (int h = 0; h < NH; ++h) alpha[h] = 1.f;
+          if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+              float bm = sc[h];
+#pragma unroll
+              for (int off = 16; off >= 1; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+              const float mn = fmaxf(m_run[h], bm);
+              alpha[h] = ex2(m_run[h] - mn);
+              m_run[h] = mn;
+              l_run[h] *= alpha[h];
+#pragma unroll
+              for (int g = 0; g < NG; ++g) pb[g][h] *= alpha[h];
+            }
+          }
+          float pr[NH];
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            pr[h] = valid ? ex2(sc[h] - m_run[h]) : 0.f;
+            l_run[h] += pr[h];
+          }
+          // p * A_v for the V warps (buffer pbuf, free once the V warps are done with tile i - 2), sums of p * B_v
+          if (i >= 2) ok = ok && wait_warp(&p_empty[pbuf], ((i >> 1) - 1) & 1, abort_flag, p.err);
+          float4* psr = ps + ((size_t)pbuf * TILE + m) * Ls.ps_row;
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            const float sv = valid ? half_bits_to_float_rt(sVS[m * NG + g], f16) : 0.f;
+            const float bv = valid ? half_bits_to_float_rt(sVB[m * NG + g], f16) : 0.f;
+            const float2 av = coeffs<4, EXACT>(sv, bv);
+            psr[g] = make_float4(pr[0] * av.x, pr[1] * av.x, pr[2] * av.x, pr[3] * av.x);
+#pragma unroll
+            for (int h = 0; h < NH; ++h) pb[g][h] = fmaf(pr[h], av.y, pb[g][h]);
+          }
+          if (lane == 0) reinterpret_cast<float4*>(alpha_s)[pbuf * 4 + q] = make_float4(alpha[0], alpha[1], alpha[2], alpha[3]);
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&p_full[pbuf]);
+            mbar_arrive(&vempty[vs]);
+          }
+          if (c1 == walk.u_end || c1 == r1) {
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+              for (int h = 0; h < NH; ++h) {
+                l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], off);
+#pragma unroll
+                for (int g = 0; g < NG; ++g) pb[g][h] += __shfl_xor_sync(0xffffffffu, pb[g][h], off);
+              }
+            }
+            named_barrier_sync(1, EV_THREADS);   // the V warps are past this tile: the area is free
+            if (lane == 0) {
+#pragma unroll
+              for (int h = 0; h < NH; ++h) {
+                cm[q * NH + h] = m_run[h];
+                cl[q * NH + h] = l_run[h];
+#pragma unroll
+                for (int g = 0; g < NG; ++g) cpb[(q * NG + g) * NH + h] = pb[g][h];
+              }
+            }
+            combine(walk.unit);
+            if (lane == 0) mbar_arrive(&qs_free[uidx & 1]);
+            reset();
+          }
+          ++i;
+          if (++vs == VS) {
+            vs = 0;
+            vph ^= 1;
+          }
+        }
+      } else {
+        // ------------------------------------------------------------------------------ V warps
+        const int vw = warp - V0;   // rows 16 vw .. 16 vw + 15 of every tile
+        const int vlane = lane % VL, vrow = lane / VL;
+        const int gv = (vlane * EV) / GS;
+        float2 o[NH][EV / 2];
+        auto reset = [&]() {
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+#pragma unroll
+            for (int k = 0; k < EV / 2; ++k) o[h][k] = make_float2(0.f, 0.f);
+        };
+        reset();
+        while (walk.next(p, c0, c1, t0)) {
+          const unsigned char* vst = smem + Ls.v0 + (size_t)vs * Ls.vstage_bytes;
+          const int lr0 = (int)(c0 - t0), lr1 = (int)(c1 - t0);
+          const int pbuf = i & 1;
+          ok = ok && wait_warp(&p_full[pbuf], (i >> 1) & 1, abort_flag, p.err);
+          ok = ok && wait_warp(&vfull[vs], vph, abort_flag, p.err);
+          const float4 al4 = reinterpret_cast<const float4*>(alpha_s)[pbuf * 4 + q];
+          const float al[4] = {al4.x, al4.y, al4.z, al4.w};
+          if (al[0] != 1.f || al[1] != 1.f || al[2] != 1.f || al[3] != 1.f) {
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+#pragma unroll
+              for (int k = 0; k < EV / 2; ++k) o[h][k] = __fmul2_rn(o[h][k], make_float2(al[h], al[h]));
+          }
+          if (ok && 16 * vw < lr1 && 16 * vw + 16 > lr0) {
+            // this warp's 16 rows of the tile (rows outside the chunk carry p * A_v = 0)
+            const uint32_t* sV = reinterpret_cast<const uint32_t*>(vst);
+            const float4* pp = ps + (size_t)pbuf * TILE * Ls.ps_row + gv;
+#pragma unroll 2
+            for (int rs = 0; rs < 16 / VR; ++rs) {
+              const int r = 16 * vw + rs * VR + vrow;
+              uint32_t w[VW];
+              load_words<VW>(sV + r * W + vlane * VW, w);
+              float2 f[EV / 2];
+              unpack_words<4, EXACT, VW>(w, f);
+              const float4 a4 = pp[r * Ls.ps_row];
+              const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+              for (int h = 0; h < NH; ++h)
+#pragma unroll
+                for (int k = 0; k < EV / 2; ++k) o[h][k] = __ffma2_rn(make_float2(av[h], av[h]), f[k], o[h][k]);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&p_empty[pbuf]);
+            mbar_arrive(&vempty[vs]);
+          }
+          if (c1 == walk.u_end || c1 == r1) {
+            if constexpr (VR > 1) {   // the lanes of one V slice took different rows: add their sums
+#pragma unroll
+              for (int off = VL; off < 32; off <<= 1)
+#pragma unroll
+                for (int h = 0; h < NH; ++h)
+#pragma unroll
+                  for (int k = 0; k < EV / 2; ++k)
+                    o[h][k] = __fadd2_rn(o[h][k], make_float2(__shfl_xor_sync(0xffffffffu, o[h][k].x, off),
+                                                              __shfl_xor_sync(0xffffffffu, o[h][k].y, off)));
+            }
+            named_barrier_sync(1, EV_THREADS);   // the epilogue warps are past this tile: the area is free
+            if (vrow == 0) {
+#pragma unroll
+              for (int h = 0; h < NH; ++h)
+#pragma unroll
+                for (int k = 0; k < EV / 2; ++k)
+                  reinterpret_cast<float2*>(co + (vw * NH + h) * D + vlane * EV)[k] = o[h][k];
+            }
+            combine(walk.unit);
+            reset();
+          }
+          ++i;
+          if (++vs == VS) {
+            vs = 0;
+            vph ^= 1;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tbase, TMEM_COLS);
+  }
+}
+
+template <bool EXACT, typename Fn>
+cudaError_t with_tc_kernel(int D, int nh, int ng, Fn&& f) {
+#define QDA_TC(D_, NG_) \
+  if (D == D_ && nh == 4 && ng == NG_) return f(qda_tc_kernel<D_, 4, NG_, EXACT>);
+  QDA_TC(128, 2) QDA_TC(128, 4) QDA_TC(256, 2) QDA_TC(256, 4) QDA_TC(256, 8)
+#undef QDA_TC
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace qda

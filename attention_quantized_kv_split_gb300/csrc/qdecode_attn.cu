@@ -5,6 +5,9 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <vector>
+
+#include <cuda.h>
 
 #include "qda_internal.h"
 
@@ -12,7 +15,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr long long kMinRowsPerCta = 128;
-constexpr long long kMaxCtas = 4096;   // the merge kernel stages one weight per partial in shared memory
+constexpr long long kMaxCtas = 4096;   // plan cap: CTA row ranges use a 64-bit magic division exact up to here
 
 thread_local int t_last_cuda_error = 0;
 thread_local void* t_split_event = nullptr;
@@ -29,6 +32,7 @@ struct DeviceState {
   unsigned int* err = nullptr;      // address of g_device_err on this device
   void* ws = nullptr;               // library-owned workspace
   size_t ws_bytes = 0;
+  std::vector<void*> retired;       // outgrown workspaces, kept allocated until the process ends
   void* user_ws = nullptr;          // caller-installed workspace
   size_t user_ws_bytes = 0;
   std::map<std::tuple<int, int, int, int, int, size_t>, int> occupancy;
@@ -90,6 +94,9 @@ int check_dtype(int dtype, int* in, int* out) {
 struct Variant {
   int W, nh, hc, heads_pad, NG, tile, stages;   // words per row, heads per CTA, head chunks, ..., ring stages
   size_t smem;
+  bool tc = false;                              // the tensor-core split kernel (qda_tc.cuh)
+  int threads = QDA_THREADS;
+  int kstages = 0;                              // tensor-core kernel: K-ring depth (stages: V-ring depth)
 };
 
 constexpr size_t kSmemBudget = 112 * 1024;   // two CTAs per SM
@@ -117,7 +124,38 @@ Variant pick_variant(int nrep, int D, int GS, int bits) {
   return v;
 }
 
+constexpr size_t kTcSmemBudget = 227 * 1024;   // one CTA per SM
+constexpr long long kTcMaxRows = (1LL << 31) - 2 * QDA_TC_TILE;   // tensor-copy row coordinates are int32
+
+// The tensor-core kernel serves single-query decode of 4-bit caches at D = 128 and 256 with at least two groups
+// per row and three or more query heads per KV head (four per CTA); T is the cache's total row count.
+bool tc_eligible(int nrep, int D, int GS, int bits, long long T) {
+  return bits == 4 && (D == 128 || D == 256) && D / GS >= 2 && nrep >= 3 && T <= kTcMaxRows;
+}
+
+Variant pick_tc_variant(int nrep, int D, int GS) {
+  Variant v;
+  v.tc = true;
+  v.threads = QDA_TC_THREADS;
+  v.W = D / 8;
+  v.NG = D / GS;
+  v.nh = 4;
+  v.hc = (nrep + 3) / 4;
+  v.heads_pad = v.hc * 4;
+  v.tile = QDA_TC_TILE;
+  // K ring: three tiles (one being converted, two in flight); V ring: the rest of shared memory, 3 to 12 tiles
+  v.kstages = 3;
+  const QdaTcLayout L0 = qda_tc_layout(D, 4, v.NG, v.kstages, 0);
+  const long long st = ((long long)kTcSmemBudget - (long long)L0.total) / (long long)L0.vstage_bytes;
+  v.stages = (int)std::max(3LL, std::min(12LL, st));
+  v.smem = qda_tc_layout(D, 4, v.NG, v.kstages, v.stages).total;
+  return v;
+}
+
 cudaError_t split_occupancy(int bits, int D, bool exact, const Variant& v, int* n) {
+  if (v.tc) {
+    return exact ? qda_occupancy_tc_x1(D, v.nh, v.NG, v.smem, n) : qda_occupancy_tc_x0(D, v.nh, v.NG, v.smem, n);
+  }
   if (bits == 4) {
     return exact ? qda_occupancy_split2_b4_x1(D, v.nh, v.NG, v.smem, n)
                  : qda_occupancy_split2_b4_x0(D, v.nh, v.NG, v.smem, n);
@@ -154,7 +192,7 @@ void make_plan(int B, int Hkv, const int32_t* N, int D, int num_sms, int ctas_pe
   plan->heads_per_cta = v.nh;
   plan->tile_rows = v.tile;
   plan->stages = v.stages;
-  plan->threads = QDA_THREADS;
+  plan->threads = v.threads;
   plan->units = units;
   plan->smem_bytes = (int)v.smem;
   plan->total_rows = T;
@@ -188,7 +226,7 @@ DeviceState* device_state(int* dev_out) {
 
 int occupancy_for(DeviceState& d, int bits, int D, bool exact, const Variant& v, int* n) {
   std::lock_guard<std::mutex> lock(d.mu);
-  auto key = std::make_tuple(bits + 16 * (int)exact, D, 0, v.nh, v.NG, v.smem);
+  auto key = std::make_tuple(bits + 16 * (int)exact, D, (int)v.tc, v.nh, v.NG, v.smem);
   auto it = d.occupancy.find(key);
   if (it != d.occupancy.end()) {
     *n = it->second;
@@ -209,12 +247,53 @@ static __device__ __align__(256) unsigned char g_qda_static_scratch[QDA_STATIC_S
 std::mutex g_static_mu;
 void* g_static_scratch_addr[kMaxDevices] = {};
 
+// The 2-D tensor map of a cache's K codes for the tensor-core kernel: rows of D / 2 bytes, boxes of 128 rows by
+// min(D / 2, 128) bytes, 16-byte chunks swizzled within 128-byte (64-byte at D = 128) rows so that one thread per
+// row reads shared memory without bank conflicts. cuTensorMapEncodeTiled comes from the driver through the runtime.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+cudaError_t encode_k_map(const uint32_t* k_packed, int D, long long rows, CUtensorMap* map) {
+  static EncodeTiledFn fn = nullptr;
+  static cudaError_t fn_status = cudaSuccess;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    fn_status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+    if (fn_status == cudaSuccess && (q != cudaDriverEntryPointSuccess || f == nullptr))
+      fn_status = cudaErrorSymbolNotFound;
+    fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  if (fn_status != cudaSuccess) return fn_status;
+  const cuuint64_t rb = (cuuint64_t)D / 2;
+  const cuuint64_t dims[2] = {rb, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {rb};
+  const cuuint32_t box[2] = {(cuuint32_t)std::min<cuuint64_t>(rb, 128), (cuuint32_t)QDA_TC_TILE};
+  const cuuint32_t elem[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t*>(k_packed), dims, strides, box,
+                        elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        rb >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The split kernel a call takes: the tensor-core kernel for single-query decode where it applies, else the lean
+// CUDA-core kernel (every shape, multi-query decode and the compat form).
+Variant choose_variant(int B, int L, int nrep, int Hkv, const int32_t* N, int D, int GS, int bits, bool compat) {
+  long long T = 0;
+  for (int b = 0; b < B; ++b) T += (long long)N[b] * Hkv;
+  if (L == 1 && !compat && tc_eligible(nrep, D, GS, bits, T)) return pick_tc_variant(nrep, D, GS);
+  return pick_variant(nrep * L, D, GS, bits);
+}
+
 int plan_impl(int B, int L, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int num_sms, int ctas_per_sm,
               qda_plan* plan) {
   if (plan == nullptr) return QDA_ERR_INVALID;
   int st = check_shape(B, L, H, Hkv, N, D, GS, bits);
   if (st != QDA_OK) return st;
-  const Variant v = pick_variant((H / Hkv) * L, D, GS, bits);
+  const Variant v = choose_variant(B, L, H / Hkv, Hkv, N, D, GS, bits, false);
   if (num_sms <= 0 || ctas_per_sm <= 0) {
     int dev;
     DeviceState* d = device_state(&dev);
@@ -251,8 +330,8 @@ int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, cons
     if (!aligned16(ptr)) return QDA_ERR_ALIGN;
 
   const int nrep = H / Hkv;
-  const Variant v = pick_variant(nrep * L, D, GS, bits);
   if (compat && L != 1) return QDA_ERR_UNSUPPORTED;
+  const Variant v = choose_variant(B, L, nrep, Hkv, N, D, GS, bits, compat);
   int dev;
   DeviceState* d = device_state(&dev);
   if (d == nullptr) return QDA_ERR_CUDA;
@@ -281,12 +360,14 @@ int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, cons
       ws = d->user_ws;
     } else {
       if (d->ws_bytes < plan.workspace_bytes) {
-        if (d->ws != nullptr) cudaFree(d->ws);
-        d->ws = nullptr;
-        d->ws_bytes = 0;
-        const size_t want = std::max(plan.workspace_bytes, (size_t)1 << 20);
-        cudaError_t e = cudaMalloc(&d->ws, want);
+        // grow (at least doubling); the smaller buffer is retired, not freed: a CUDA graph captured earlier or a
+        // launch another thread is about to make may still write to it
+        const size_t want = std::max({plan.workspace_bytes, 2 * d->ws_bytes, (size_t)1 << 20});
+        void* grown = nullptr;
+        cudaError_t e = cudaMalloc(&grown, want);
         if (e != cudaSuccess) return cuda_fail(e);
+        if (d->ws != nullptr) d->retired.push_back(d->ws);
+        d->ws = grown;
         d->ws_bytes = want;
       }
       ws = d->ws;
@@ -322,6 +403,7 @@ int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, cons
   p.num_ctas = plan.num_ctas;
   p.tile_rows = v.tile;
   p.stages = v.stages;
+  p.kstages = v.kstages;
   p.tile_shift = 0;
   while ((1 << p.tile_shift) < v.tile) ++p.tile_shift;
   p.f16 = in_dt == QDA_FP16 ? 1 : 0;
@@ -345,7 +427,15 @@ int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, cons
   } else {
     p.mode = L > 1 ? 1 : 0;
   }
-  e = split_launch(bits, exact, p, v, grid, s);
+  if (v.tc) {
+    CUtensorMap tmk;
+    e = encode_k_map(k_packed, D, plan.total_rows, &tmk);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = exact ? qda_launch_tc_x1(p, &tmk, D, v.nh, v.NG, grid, v.smem, s)
+              : qda_launch_tc_x0(p, &tmk, D, v.nh, v.NG, grid, v.smem, s);
+  } else {
+    e = split_launch(bits, exact, p, v, grid, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e);
   const bool use_event = t_split_event != nullptr && where == Scratch::kWorkspace;
   if (use_event) {
@@ -382,10 +472,27 @@ int qdecode_attn_multi_plan(int B, int L, int H, int Hkv, const int32_t* N, int 
 
 int qdecode_attn_workspace_bytes(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, size_t* bytes) {
   if (bytes == nullptr) return QDA_ERR_INVALID;
-  qda_plan plan;
-  const int st = plan_impl(B, 1, H, Hkv, N, D, GS, bits, 0, 0, &plan);
+  int st = check_shape(B, 1, H, Hkv, N, D, GS, bits);
   if (st != QDA_OK) return st;
-  *bytes = plan.workspace_bytes;
+  int dev;
+  DeviceState* d = device_state(&dev);
+  if (d == nullptr) return QDA_ERR_CUDA;
+  // the largest need of every call of this shape: qdecode_attn (tensor-core or lean kernel) and qdecode_attn_compat,
+  // each with 16-bit or fp32 output (the output form selects a kernel instance whose occupancy can differ)
+  const int nrep = H / Hkv;
+  const Variant vs[2] = {choose_variant(B, 1, nrep, Hkv, N, D, GS, bits, false), pick_variant(nrep, D, GS, bits)};
+  size_t most = 0;
+  for (const Variant& v : vs) {
+    for (int exact = 0; exact < 2; ++exact) {
+      int occ = 1;
+      st = occupancy_for(*d, bits, D, exact != 0, v, &occ);
+      if (st != QDA_OK) return st;
+      qda_plan plan;
+      make_plan(B, Hkv, N, D, d->num_sms, occ, v, &plan);
+      most = std::max(most, plan.workspace_bytes);
+    }
+  }
+  *bytes = most;
   return QDA_OK;
 }
 

@@ -70,7 +70,15 @@ extern "C" {
  * synchronises. N is a HOST array of B lengths (N[b] >= 1). The call reads q and the cache, writes out, and uses
  * a workspace of qdecode_attn_workspace_bytes() bytes: the library's own per-device buffer (allocated or grown
  * with cudaMalloc on first need, which synchronises the device) unless one was installed with
- * qdecode_attn_set_workspace(). Calls that share one workspace must not overlap on the GPU.
+ * qdecode_attn_set_workspace(). Calls that share one workspace must not overlap on the GPU. When the library's
+ * buffer grows, the smaller one is kept allocated (not freed) until the process ends, so a CUDA graph captured
+ * before the growth still writes to valid memory; a captured call can also use an installed workspace or
+ * qdecode_attn_noalloc, whose scratch never moves.
+ *
+ * Kernels: for 4-bit caches with D = 128 or 256, at least two groups per row and three or more query heads per KV
+ * head, the scores of each 128-row tile are computed on the tensor cores (tcgen05: codes as exact 16-bit values
+ * 128 + c (bf16) or 1024 + c (fp16), q in its own 16-bit dtype, fp32 accumulation per group); every other shape,
+ * and the V side everywhere, runs on CUDA cores in fp32.
  */
 int qdecode_attn(const void* q, const uint32_t* k_packed, const void* k_scales, const void* k_biases,
                  const uint32_t* v_packed, const void* v_scales, const void* v_biases, void* out,
@@ -179,7 +187,8 @@ int qdecode_attn_plan(int B, int H, int Hkv, const int32_t* N, int D, int GS, in
 int qdecode_attn_multi_plan(int B, int L, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int num_sms,
                             int ctas_per_sm, qda_plan* plan);
 
-/* Workspace size in bytes qdecode_attn needs for this shape on the current device. */
+/* Workspace size in bytes that qdecode_attn and qdecode_attn_compat need for this shape on the current device,
+   whatever the dtype argument (the largest over the kernels those calls can take). */
 int qdecode_attn_workspace_bytes(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, size_t* bytes);
 
 /*
