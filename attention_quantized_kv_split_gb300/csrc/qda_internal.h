@@ -120,18 +120,27 @@ __host__ __device__ inline int split2_scratch_floats(int R, int NG, int NH) {
 #define QDA_TC_THREADS (QDA_TC_WARPS * 32)
 #define QDA_TC_TILE 128   // rows per pipeline tile: the M of every MMA
 
+// Bytes of codes per ring slot of the tensor-core kernel: a slot of 32 KB of K codes (and one of V codes) holds
+// 32768 / (D / 2) rows, several 128-row MMA tiles. The size is the point: bulk copies that complete a barrier phase
+// per 16 KB stream the cache at about 4 TB/s on GB300, per 32 KB or more at about 7 TB/s.
+#define QDA_TC_SLOT_BYTES 32768
+
+// Rows per ring slot for head dimension D (4-bit codes: D / 2 bytes per row).
+__host__ __device__ inline int qda_tc_slot_rows(int D) { return QDA_TC_SLOT_BYTES / (D / 2); }
+
 // Shared-memory layout of the tensor-core split kernel for one (D, heads per CTA, groups per row) and ring depths:
-// a ring of K-code tiles (kept until converted) and a ring of V-code + scale/bias tiles (kept until the scores and
-// the V rows are done).
+// a ring of K-code slots (kept until converted) and a ring of V-code + scale/bias slots (kept until the scores and
+// the V rows of every tile of the slot are done; a slot that ends a segment also serves as its combine area).
 struct QdaTcLayout {
   size_t b_op;         // [2] B operand: q of a unit's heads, 16 x D 16-bit values in K-major core matrices
   size_t qs;           // [2][NG][NH] fp32 sums of q per group
   size_t alpha;        // [2][4][NH] fp32 rescale factors per tile, lane quarter and head
-  size_t ps;           // [2][128][ps_row] float4: p * A_v per (row, group), four heads; also the combine area
+  size_t ps;           // [2][128][ps_row] float4: p * A_v per (row, group), four heads
   int ps_row;          // float4 per row of ps (NG, plus one against bank conflicts)
-  size_t k_bytes;      // one K tile (tile rows x D / 2 bytes, 16-byte chunks swizzled by the tensor copy)
-  size_t v_bytes;      // V codes of one tile
-  size_t sc_bytes;     // one scale or bias array of a tile (tile rows x NG 16-bit values, 16-byte multiple)
+  int slot_rows;       // rows per ring slot
+  size_t k_bytes;      // one K slot (slot rows x D / 2 bytes, 16-byte chunks swizzled by the tensor copy)
+  size_t v_bytes;      // V codes of one slot
+  size_t sc_bytes;     // one scale or bias array of a slot (slot rows x NG 16-bit values, 16-byte multiple)
   size_t vstage_bytes; // V codes, K scales, K biases, V scales, V biases
   size_t k0, v0;       // offsets of the K ring (1024-byte aligned: the swizzle follows address bits 4..9) and V ring
   size_t total;
@@ -146,17 +155,16 @@ __host__ __device__ inline size_t qda_tc_combine_bytes(int D, int NH, int NG) {
 __host__ __device__ inline QdaTcLayout qda_tc_layout(int D, int NH, int NG, int kstages, int vstages) {
   QdaTcLayout L;
   const size_t RB = (size_t)D / 2;
+  L.slot_rows = qda_tc_slot_rows(D);
   L.b_op = 1024;   // barriers, the abort word and the tensor-memory address sit below
   L.qs = L.b_op + 2 * 32 * (size_t)D;
   L.alpha = L.qs + 2 * (size_t)NG * NH * 4;
   L.ps = (L.alpha + 2 * 4 * (size_t)NH * 4 + 15) & ~(size_t)15;
   L.ps_row = NG + 1;
-  size_t ps_bytes = 2 * (size_t)QDA_TC_TILE * L.ps_row * 16;
-  const size_t cb = qda_tc_combine_bytes(D, NH, NG);
-  if (cb > ps_bytes) ps_bytes = cb;
-  L.k_bytes = (size_t)QDA_TC_TILE * RB;
-  L.v_bytes = (size_t)QDA_TC_TILE * RB;
-  L.sc_bytes = ((size_t)QDA_TC_TILE * NG * 2 + 15) & ~(size_t)15;
+  const size_t ps_bytes = 2 * (size_t)QDA_TC_TILE * L.ps_row * 16;
+  L.k_bytes = (size_t)L.slot_rows * RB;
+  L.v_bytes = (size_t)L.slot_rows * RB;
+  L.sc_bytes = ((size_t)L.slot_rows * NG * 2 + 15) & ~(size_t)15;
   L.vstage_bytes = L.v_bytes + 4 * L.sc_bytes;
   L.k0 = (L.ps + ps_bytes + 1023) & ~(size_t)1023;
   L.v0 = L.k0 + (size_t)kstages * L.k_bytes;

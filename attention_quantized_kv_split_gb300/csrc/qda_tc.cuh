@@ -65,7 +65,7 @@ __device__ __forceinline__ void tc_issue_v(const QdaParams& p, unsigned char* vs
   const uint32_t s16 = sbytes & ~15u;
   const size_t soff = (size_t)(s0 - t0) * SB;
   unsigned char* sc = vst + L.v_bytes;
-  const bool inb = in_bounds(c0 >= t0 && c0 < c1 && c1 <= T && c1 - t0 <= QDA_TC_TILE && s1 <= T && s0 >= t0 &&
+  const bool inb = in_bounds(c0 >= t0 && c0 < c1 && c1 <= T && c1 - t0 <= L.slot_rows && s1 <= T && s0 >= t0 &&
                                  coff + cbytes <= L.v_bytes && soff + sbytes <= L.sc_bytes,
                              p.err);
   if (lane == 0 && !inb) mbar_arrive_expect_tx(full, 0);
@@ -96,11 +96,13 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
     qda_tc_kernel(const __grid_constant__ QdaParams p, const __grid_constant__ CUtensorMap tmk) {
   constexpr int TILE = QDA_TC_TILE;
   constexpr int RB = D / 2, W = D / 8, CPR = RB / 16, GS = D / NG;
+  constexpr int SLOT = QDA_TC_SLOT_BYTES / RB;   // rows per ring slot: SLOT / TILE MMA tiles
+  constexpr int BOXW = RB >= 128 ? 128 : RB;     // bytes per row of one tensor-copy box (its rows: <= 256)
+  constexpr int BOXES_Y = SLOT / 256, BOXES_X = RB / BOXW;
   constexpr int EV = D >= 256 ? D / 32 : 8, VL = D / EV, VR = 32 / VL, VW = EV / 8;
   constexpr int A_COLS = D / 2, ACC_COLS = 16 * NG;
   constexpr int TMEM_COLS = tc_tmem_cols(2 * A_COLS + 2 * ACC_COLS);
   constexpr int KSTEPS = D / 16;
-  constexpr int REGIONS = RB >= 128 ? RB / 128 : 1;
   constexpr int EPI0 = QDA_TC_CONV, V0 = EPI0 + QDA_TC_EPI, PRODUCER = V0 + QDA_TC_VW, MMA_WARP = PRODUCER + 1;
   // MMA_WARP issues the MMAs of even tiles and allocates tensor memory, MMA_WARP + 1 those of odd tiles
   constexpr int EV_THREADS = (QDA_TC_EPI + QDA_TC_VW) * 32;
@@ -108,16 +110,17 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
   static_assert(NG >= 2 && GS >= 32 && GS % 16 == 0, "two or more groups of at least 32 codes per row");
   static_assert(2 * A_COLS + 2 * ACC_COLS <= 512, "tensor memory");
   static_assert(RB == 64 || RB % 128 == 0, "K rows of 64 or 128k bytes");
+  static_assert(SLOT % 256 == 0 && BOXES_X == 1, "slots of whole 256-row boxes, one box column");
   static_assert(QDA_TC_VW * 16 == TILE && QDA_TC_CONV * 32 == TILE && QDA_TC_EPI * 32 == TILE, "warp shares");
 
   extern __shared__ __align__(1024) unsigned char smem[];
   const int KS = p.kstages, VS = p.stages;
   const QdaTcLayout Ls = qda_tc_layout(D, NH, NG, KS, VS);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* kfull = bars;          // [KS <= 8] K tile landed
-  uint64_t* kempty = bars + 8;     // [KS] K tile converted (4 converter warps)
+  uint64_t* kfull = bars;          // [KS <= 8] K slot landed
+  uint64_t* kempty = bars + 8;     // [KS] K slot converted (4 converter warps)
   uint64_t* vfull = bars + 16;     // [VS <= 12] V codes and scales landed
-  uint64_t* vempty = bars + 28;    // [VS] scales and V rows used (4 epilogue + 8 V warps)
+  uint64_t* vempty = bars + 28;    // [VS] scales and V rows of every tile of the slot used (4 epilogue + 8 V warps)
   uint64_t* a_full = bars + 40;    // [2] A buffer written (4 converter warps)
   uint64_t* a_free = bars + 42;    // [2] the MMAs that read A buffer b are complete
   uint64_t* acc_full = bars + 44;  // [2] accumulator buffer b holds the tile's sums
@@ -172,10 +175,15 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
   pdl_launch_dependents();
 
   if (r0 < r1) {
-    ChunkWalker walk;
+    ChunkWalker walk;   // chunks: a slot of SLOT rows intersected with one (sequence, KV head) and the CTA's range
     walk.init(p, r0, r1);
     long long c0, c1, t0;
     const bool f16 = p.f16 != 0;
+    // the 128-row tiles of a slot that a chunk [c0, c1) (slot rows lr0 .. lr1) touches: st0 .. st1 - 1
+    auto tiles_of = [](int lr0, int lr1, int& st0, int& st1) {
+      st0 = lr0 / TILE;
+      st1 = (lr1 + TILE - 1) / TILE;
+    };
 
     if (warp == PRODUCER) {
       // ---------------------------------------------------------------------------------- producer warp
@@ -187,8 +195,8 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
         if (lane == 0) {
           mbar_arrive_expect_tx(&kfull[ks], (uint32_t)Ls.k_bytes);
           unsigned char* kst = smem + Ls.k0 + (size_t)ks * Ls.k_bytes;
-          for (int rg = 0; rg < REGIONS; ++rg)   // the whole tile: rows past the cache read as zero
-            tma_load_2d(kst + (size_t)rg * TILE * 128, &tmk, rg * 128, (int)t0, &kfull[ks], pol);
+          for (int by = 0; by < BOXES_Y; ++by)   // the whole slot: rows past the cache read as zero
+            tma_load_2d(kst + (size_t)by * 256 * BOXW, &tmk, 0, (int)t0 + 256 * by, &kfull[ks], pol);
         }
         __syncwarp();
         if (i >= VS && !wait_warp(&vempty[vs], vph ^ 1, abort_flag, p.err)) break;
@@ -218,15 +226,22 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
       const uint64_t bdesc0 = smem_desc_kmajor(smem_addr(b_op), 256, 128);
       const uint32_t a0 = tbase + ab * A_COLS;
       const uint32_t d0 = tbase + 2 * A_COLS + ab * ACC_COLS;
-      int i = 0, uidx = -1, cur_unit = -1, issued = -1;
-      while (walk.next(p, c0, c1, t0)) {
+      int j = 0, uidx = -1, cur_unit = -1, issued = -1;
+      bool go = true;
+      while (go && walk.next(p, c0, c1, t0)) {
         if (walk.unit != cur_unit) {
           cur_unit = walk.unit;
           ++uidx;
         }
-        if ((i & 1) == ab) {
-          if (!wait_warp(&a_full[ab], (i >> 1) & 1, abort_flag, p.err)) break;
-          if (i >= 2 && !wait_warp(&acc_empty[ab], ((i >> 1) - 1) & 1, abort_flag, p.err)) break;
+        int st0, st1;
+        tiles_of((int)(c0 - t0), (int)(c1 - t0), st0, st1);
+        for (int st = st0; st < st1; ++st, ++j) {
+          if ((j & 1) != ab) continue;
+          if (!wait_warp(&a_full[ab], (j >> 1) & 1, abort_flag, p.err) ||
+              (j >= 2 && !wait_warp(&acc_empty[ab], ((j >> 1) - 1) & 1, abort_flag, p.err))) {
+            go = false;
+            break;
+          }
           tc_fence_after();
           if (lane == 0) {
             const uint64_t bd = bdesc0 + (uint64_t)((uidx & 1) * 2 * D);
@@ -239,31 +254,29 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
             mma_commit(&acc_full[ab]);
           }
           __syncwarp();
-          issued = i;
+          issued = j;
         }
-        ++i;
       }
       // every MMA this warp issued is complete before the tensor memory is freed
       if (issued >= 0 && lane == 0) mbar_wait_drain(&a_free[ab], (issued >> 1) & 1, p.err);
       __syncwarp();
     } else if (warp < EPI0) {
       // ---------------------------------------------------------------------------------- converter warps
-      const int m = 32 * warp + lane;   // the tile row this thread converts
       const uint32_t tl = tbase + ((uint32_t)(32 * warp) << 16);
       const uint32_t magic = f16 ? 0x64006400u : 0x43004300u;   // OFF + c in the low mantissa bits
-      int i = 0, ks = 0, kph = 0, uidx = -1, cur_unit = -1;
+      int i = 0, j = 0, ks = 0, kph = 0, uidx = -1, cur_unit = -1;
       bool ok = true;   // false once a wait of this warp gave up: the warp then passes every barrier with no work
       while (walk.next(p, c0, c1, t0)) {
         ok = ok && wait_warp(&kfull[ks], kph, abort_flag, p.err);
-        // A buffer i & 1 was last read by the MMAs of tile i - 2
-        if (i >= 2) ok = ok && wait_warp(&a_free[i & 1], ((i >> 1) - 1) & 1, abort_flag, p.err);
-        tc_fence_after();
         if (walk.unit != cur_unit) {
           // a new (sequence, KV head): its q into B operand buffer (unit parity) and its sums per group, once the
-          // epilogue is done with the unit two back (the MMAs that read that buffer are complete: tile i - 2)
+          // MMAs that read that buffer (two units back) are complete -- the latest MMA of each A buffer covers
+          // every earlier one of its issuer -- and the epilogue is done with those sums
           cur_unit = walk.unit;
           ++uidx;
           const int par = uidx & 1;
+          if (j >= 1) ok = ok && wait_warp(&a_free[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err);
+          if (j >= 2) ok = ok && wait_warp(&a_free[j & 1], ((j >> 1) - 1) & 1, abort_flag, p.err);
           if (uidx >= 2) ok = ok && wait_warp(&qs_free[par], ((uidx >> 1) - 1) & 1, abort_flag, p.err);
           if (ok) {
             constexpr int OCT = D / 8;
@@ -271,10 +284,10 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
             float sum = 0.f;
             if (item < NH * OCT) {
               const int h = item / OCT, wi = item - h * OCT;
-              const int j = hc * NH + h;
+              const int jq = hc * NH + h;
               uint4 a = make_uint4(0, 0, 0, 0);
-              if (j < p.nrep * p.L) {
-                const long long row = qda_q_row(walk.b, walk.kvh, j, p.nrep, p.L, p.H);
+              if (jq < p.nrep * p.L) {
+                const long long row = qda_q_row(walk.b, walk.kvh, jq, p.nrep, p.L, p.H);
                 if (in_bounds(row < (long long)p.B * p.L * p.H, p.err))
                   a = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) + row * D + 8 * wi);
               }
@@ -299,37 +312,44 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
           named_barrier_sync(2, QDA_TC_CONV * 32);
           if (lane == 0) mbar_arrive(&qs_full[par]);
         }
-        if (ok) {
-          const unsigned char* sK = smem + Ls.k0 + (size_t)ks * Ls.k_bytes;
+        int st0, st1;
+        tiles_of((int)(c0 - t0), (int)(c1 - t0), st0, st1);
+        const unsigned char* sK = smem + Ls.k0 + (size_t)ks * Ls.k_bytes;
+        for (int st = st0; st < st1; ++st, ++j) {
+          // A buffer j & 1 was last read by the MMAs of tile j - 2
+          if (j >= 2) ok = ok && wait_warp(&a_free[j & 1], ((j >> 1) - 1) & 1, abort_flag, p.err);
+          tc_fence_after();
+          if (ok) {
+            const int row = st * TILE + 32 * warp + lane;   // the slot row this thread converts
 #pragma unroll 2
-          for (int c = 0; c < CPR; ++c) {
-            const unsigned char* src;
-            if constexpr (RB == 64) {
-              src = sK + m * 64 + ((c ^ ((m >> 1) & 3)) << 4);
-            } else {
-              src = sK + (c >> 3) * (TILE * 128) + m * 128 + (((c & 7) ^ (m & 7)) << 4);
-            }
-            const uint4 x = *reinterpret_cast<const uint4*>(src);
-            const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
-            uint32_t out[16];
+            for (int c = 0; c < CPR; ++c) {
+              const unsigned char* src;
+              if constexpr (RB == 64) {
+                src = sK + row * 64 + ((c ^ ((row >> 1) & 3)) << 4);
+              } else {
+                src = sK + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+              }
+              const uint4 x = *reinterpret_cast<const uint4*>(src);
+              const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+              uint32_t out[16];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              // column 4 w + j of word w holds (code j, code j + 4) of the word as (low, high) halves
-              out[4 * t + 0] = (wv[t] & 0x000F000Fu) | magic;
-              out[4 * t + 1] = ((wv[t] >> 4) & 0x000F000Fu) | magic;
-              out[4 * t + 2] = ((wv[t] >> 8) & 0x000F000Fu) | magic;
-              out[4 * t + 3] = ((wv[t] >> 12) & 0x000F000Fu) | magic;
+              for (int t = 0; t < 4; ++t) {
+                // column 4 w + j of word w holds (code j, code j + 4) of the word as (low, high) halves
+                out[4 * t + 0] = (wv[t] & 0x000F000Fu) | magic;
+                out[4 * t + 1] = ((wv[t] >> 4) & 0x000F000Fu) | magic;
+                out[4 * t + 2] = ((wv[t] >> 8) & 0x000F000Fu) | magic;
+                out[4 * t + 3] = ((wv[t] >> 12) & 0x000F000Fu) | magic;
+              }
+              tmem_st16(tl + (j & 1) * A_COLS + 16 * c, out);
             }
-            tmem_st16(tl + (i & 1) * A_COLS + 16 * c, out);
+            tmem_wait_st();
           }
-          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[j & 1]);
         }
-        tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&kempty[ks]);
-          mbar_arrive(&a_full[i & 1]);
-        }
+        if (lane == 0) mbar_arrive(&kempty[ks]);
         ++i;
         if (++ks == KS) {
           ks = 0;
@@ -339,16 +359,15 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
     } else {
       // ---------------------------------------------------------------------------- epilogue and V warps
       const bool epi = warp < V0;
-      const int q = epi ? warp - EPI0 : (warp - V0) >> 1;   // lane quarter (rows 32 q .. 32 q + 31)
+      const int q = epi ? warp - EPI0 : (warp - V0) >> 1;   // lane quarter (rows 32 q .. 32 q + 31 of a tile)
       const int ev_tid = threadIdx.x - EPI0 * 32;
-      float* co = reinterpret_cast<float*>(smem + Ls.ps);   // segment-end combine area (the p * A_v buffers)
-      float* cm = co + QDA_TC_VW * NH * D;
-      float* cl = cm + 4 * NH;
-      float* cpb = cl + 4 * NH;
-      // End of a segment, after both roles wrote their parts: one partial (max, sum, o[D]) per head from the four
-      // lane quarters, combined in a fixed order by the 384 epilogue and V threads. The area is free: the V warps
-      // are past this tile and the epilogue warps have not started the next.
-      auto combine = [&](int unit) {
+      // End of a segment, after both roles wrote their parts into the chunk's V slot (the combine area; its copies
+      // have landed and both roles are done with it): one partial (max, sum, o[D]) per head from the four lane
+      // quarters, combined in a fixed order by the 384 epilogue and V threads.
+      auto combine = [&](float* co, int unit) {
+        const float* cm = co + QDA_TC_VW * NH * D;
+        const float* cl = cm + 4 * NH;
+        const float* cpb = cl + 4 * NH;
         named_barrier_sync(1, EV_THREADS);
         const long long slot = (long long)cta + unit;
         for (int idx = ev_tid; idx < NH * D; idx += EV_THREADS) {
@@ -371,14 +390,14 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
           p.part_o[hp * D + d] = O;
           if (d == 0) p.part_ml[hp] = make_float2(M, Lsum);
         }
+        fence_proxy_async();   // these generic writes to the slot come before the copies that refill it
         named_barrier_sync(1, EV_THREADS);
       };
-      int i = 0, vs = 0, vph = 0;
-      bool ok = true;   // false once a wait of this warp gave up: the warp then passes every barrier with no work
+      int i = 0, j = 0, vs = 0, vph = 0;
+      bool ok = true;
 
       if (epi) {
         // ------------------------------------------------------------------------------ epilogue warps
-        const int m = 32 * q + lane;   // the row this thread scores
         const uint32_t tl = tbase + ((uint32_t)(32 * q) << 16);
         const float OFF = f16 ? 1024.f : 128.f;
         // reference max, sum of weights and sums of p * B_v over this thread's rows, per head
@@ -396,99 +415,103 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
         reset();
         int uidx = -1, cur_unit = -1;
         while (walk.next(p, c0, c1, t0)) {
-          const unsigned char* vst = smem + Ls.v0 + (size_t)vs * Ls.vstage_bytes;
+          unsigned char* vst = smem + Ls.v0 + (size_t)vs * Ls.vstage_bytes;
           const int lr0 = (int)(c0 - t0), lr1 = (int)(c1 - t0);
-          const int pbuf = i & 1;
           if (walk.unit != cur_unit) {
             cur_unit = walk.unit;
             ++uidx;
             ok = ok && wait_warp(&qs_full[uidx & 1], (uidx >> 1) & 1, abort_flag, p.err);
           }
           const float* qs = qs_all + (uidx & 1) * NG * NH;
-          ok = ok && wait_warp(&acc_full[pbuf], (i >> 1) & 1, abort_flag, p.err);
-          tc_fence_after();
-          float acc[NG][NH];
-          if (ok) {
-#pragma unroll
-            for (int g = 0; g < NG; ++g) tmem_ld<NH>(tl + 2 * A_COLS + pbuf * ACC_COLS + 16 * g, acc[g]);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int g = 0; g < NG; ++g)
-#pragma unroll
-              for (int h = 0; h < NH; ++h) acc[g][h] = 0.f;
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[pbuf]);
           ok = ok && wait_warp(&vfull[vs], vph, abort_flag, p.err);
           const uint16_t* sKS = reinterpret_cast<const uint16_t*>(vst + Ls.v_bytes);
           const uint16_t* sKB = sKS + Ls.sc_bytes / 2;
           const uint16_t* sVS = sKB + Ls.sc_bytes / 2;
           const uint16_t* sVB = sVS + Ls.sc_bytes / 2;
-          const bool valid = m >= lr0 && m < lr1;
-          float sc[NH];
+          int st0, st1;
+          tiles_of(lr0, lr1, st0, st1);
+          for (int st = st0; st < st1; ++st, ++j) {
+            const int pbuf = j & 1;
+            ok = ok && wait_warp(&acc_full[pbuf], (j >> 1) & 1, abort_flag, p.err);
+            tc_fence_after();
+            float acc[NG][NH];
+            if (ok) {
 #pragma unroll
-          for (int h = 0; h < NH; ++h) sc[h] = 0.f;
+              for (int g = 0; g < NG; ++g) tmem_ld<NH>(tl + 2 * A_COLS + pbuf * ACC_COLS + 16 * g, acc[g]);
+              tmem_wait_ld();
+            } else {
 #pragma unroll
-          for (int g = 0; g < NG; ++g) {
-            const float s = half_bits_to_float_rt(sKS[m * NG + g], f16);
-            const float b = half_bits_to_float_rt(sKB[m * NG + g], f16);
-            const float S = p.qscale * s;
-            const float Bc = p.qscale * fmaf(-OFF, s, b);
-            const float4 q4 = reinterpret_cast<const float4*>(qs)[g];
-            const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+              for (int g = 0; g < NG; ++g)
 #pragma unroll
-            for (int h = 0; h < NH; ++h) sc[h] = fmaf(S, acc[g][h], fmaf(Bc, qv[h], sc[h]));
-          }
-          bool need = false;
+                for (int h = 0; h < NH; ++h) acc[g][h] = 0.f;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[pbuf]);
+            const int m = 32 * q + lane;     // the tile row this thread scores
+            const int row = st * TILE + m;   // its slot row
+            const bool valid = row >= lr0 && row < lr1;
+            float sc[NH];
 #pragma unroll
-          for (int h = 0; h < NH; ++h) {
-            if (!valid) sc[h] = -INFINITY;
-            need |= sc[h] > m_run[h] + 8.f;
-          }
-          // lazy rescaling: the reference max of a head moves only when a score passes it by more than 8 (a
-          // factor 2^8 in the weights)
-          float alpha[NH];
+            for (int h = 0; h < NH; ++h) sc[h] = 0.f;
 #pragma unroll
-          for (int h = 0; h < NH; ++h) alpha[h] = 1.f;
-          if (__any_sync(0xffffffffu, need)) {
+            for (int g = 0; g < NG; ++g) {
+              const float s = half_bits_to_float_rt(sKS[row * NG + g], f16);
+              const float b = half_bits_to_float_rt(sKB[row * NG + g], f16);
+              const float S = p.qscale * s;
+              const float Bc = p.qscale * fmaf(-OFF, s, b);
+              const float4 q4 = reinterpret_cast<const float4*>(qs)[g];
+              const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+              for (int h = 0; h < NH; ++h) sc[h] = fmaf(S, acc[g][h], fmaf(Bc, qv[h], sc[h]));
+            }
+            bool need = false;
 #pragma unroll
             for (int h = 0; h < NH; ++h) {
-              float bm = sc[h];
-#pragma unroll
-              for (int off = 16; off >= 1; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
-              const float mn = fmaxf(m_run[h], bm);
-              alpha[h] = ex2(m_run[h] - mn);
-              m_run[h] = mn;
-              l_run[h] *= alpha[h];
-#pragma unroll
-              for (int g = 0; g < NG; ++g) pb[g][h] *= alpha[h];
+              if (!valid) sc[h] = -INFINITY;
+              need |= sc[h] > m_run[h] + 8.f;
             }
-          }
-          float pr[NH];
+            // lazy rescaling: the reference max of a head moves only when a score passes it by more than 8 (a
+            // factor 2^8 in the weights)
+            float alpha[NH];
 #pragma unroll
-          for (int h = 0; h < NH; ++h) {
-            pr[h] = valid ? ex2(sc[h] - m_run[h]) : 0.f;
-            l_run[h] += pr[h];
-          }
-          // p * A_v for the V warps (buffer pbuf, free once the V warps are done with tile i - 2), sums of p * B_v
-          if (i >= 2) ok = ok && wait_warp(&p_empty[pbuf], ((i >> 1) - 1) & 1, abort_flag, p.err);
-          float4* psr = ps + ((size_t)pbuf * TILE + m) * Ls.ps_row;
+            for (int h = 0; h < NH; ++h) alpha[h] = 1.f;
+            if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-          for (int g = 0; g < NG; ++g) {
-            const float sv = valid ? half_bits_to_float_rt(sVS[m * NG + g], f16) : 0.f;
-            const float bv = valid ? half_bits_to_float_rt(sVB[m * NG + g], f16) : 0.f;
-            const float2 av = coeffs<4, EXACT>(sv, bv);
-            psr[g] = make_float4(pr[0] * av.x, pr[1] * av.x, pr[2] * av.x, pr[3] * av.x);
+              for (int h = 0; h < NH; ++h) {
+                float bm = sc[h];
 #pragma unroll
-            for (int h = 0; h < NH; ++h) pb[g][h] = fmaf(pr[h], av.y, pb[g][h]);
-          }
-          if (lane == 0) reinterpret_cast<float4*>(alpha_s)[pbuf * 4 + q] = make_float4(alpha[0], alpha[1], alpha[2], alpha[3]);
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&p_full[pbuf]);
-            mbar_arrive(&vempty[vs]);
+                for (int off = 16; off >= 1; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+                const float mn = fmaxf(m_run[h], bm);
+                alpha[h] = ex2(m_run[h] - mn);
+                m_run[h] = mn;
+                l_run[h] *= alpha[h];
+#pragma unroll
+                for (int g = 0; g < NG; ++g) pb[g][h] *= alpha[h];
+              }
+            }
+            float pr[NH];
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+              pr[h] = valid ? ex2(sc[h] - m_run[h]) : 0.f;
+              l_run[h] += pr[h];
+            }
+            // p * A_v for the V warps (buffer pbuf, free once the V warps are done with tile j - 2), sums of p * B_v
+            if (j >= 2) ok = ok && wait_warp(&p_empty[pbuf], ((j >> 1) - 1) & 1, abort_flag, p.err);
+            float4* psr = ps + ((size_t)pbuf * TILE + m) * Ls.ps_row;
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+              const float sv = valid ? half_bits_to_float_rt(sVS[row * NG + g], f16) : 0.f;
+              const float bv = valid ? half_bits_to_float_rt(sVB[row * NG + g], f16) : 0.f;
+              const float2 av = coeffs<4, EXACT>(sv, bv);
+              psr[g] = make_float4(pr[0] * av.x, pr[1] * av.x, pr[2] * av.x, pr[3] * av.x);
+#pragma unroll
+              for (int h = 0; h < NH; ++h) pb[g][h] = fmaf(pr[h], av.y, pb[g][h]);
+            }
+            if (lane == 0)
+              reinterpret_cast<float4*>(alpha_s)[pbuf * 4 + q] = make_float4(alpha[0], alpha[1], alpha[2], alpha[3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[pbuf]);
           }
           if (c1 == walk.u_end || c1 == r1) {
 #pragma unroll
@@ -500,8 +523,12 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
                 for (int g = 0; g < NG; ++g) pb[g][h] += __shfl_xor_sync(0xffffffffu, pb[g][h], off);
               }
             }
-            named_barrier_sync(1, EV_THREADS);   // the V warps are past this tile: the area is free
+            float* co = reinterpret_cast<float*>(vst);
+            named_barrier_sync(1, EV_THREADS);   // the V warps are past this slot: it is free
             if (lane == 0) {
+              float* cm = co + QDA_TC_VW * NH * D;
+              float* cl = cm + 4 * NH;
+              float* cpb = cl + 4 * NH;
 #pragma unroll
               for (int h = 0; h < NH; ++h) {
                 cm[q * NH + h] = m_run[h];
@@ -510,10 +537,12 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
                 for (int g = 0; g < NG; ++g) cpb[(q * NG + g) * NH + h] = pb[g][h];
               }
             }
-            combine(walk.unit);
+            combine(co, walk.unit);
             if (lane == 0) mbar_arrive(&qs_free[uidx & 1]);
             reset();
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&vempty[vs]);
           ++i;
           if (++vs == VS) {
             vs = 0;
@@ -534,42 +563,43 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
         };
         reset();
         while (walk.next(p, c0, c1, t0)) {
-          const unsigned char* vst = smem + Ls.v0 + (size_t)vs * Ls.vstage_bytes;
+          unsigned char* vst = smem + Ls.v0 + (size_t)vs * Ls.vstage_bytes;
           const int lr0 = (int)(c0 - t0), lr1 = (int)(c1 - t0);
-          const int pbuf = i & 1;
-          ok = ok && wait_warp(&p_full[pbuf], (i >> 1) & 1, abort_flag, p.err);
           ok = ok && wait_warp(&vfull[vs], vph, abort_flag, p.err);
-          const float4 al4 = reinterpret_cast<const float4*>(alpha_s)[pbuf * 4 + q];
-          const float al[4] = {al4.x, al4.y, al4.z, al4.w};
-          if (al[0] != 1.f || al[1] != 1.f || al[2] != 1.f || al[3] != 1.f) {
-#pragma unroll
-            for (int h = 0; h < NH; ++h)
-#pragma unroll
-              for (int k = 0; k < EV / 2; ++k) o[h][k] = __fmul2_rn(o[h][k], make_float2(al[h], al[h]));
-          }
-          if (ok && 16 * vw < lr1 && 16 * vw + 16 > lr0) {
-            // this warp's 16 rows of the tile (rows outside the chunk carry p * A_v = 0)
-            const uint32_t* sV = reinterpret_cast<const uint32_t*>(vst);
-            const float4* pp = ps + (size_t)pbuf * TILE * Ls.ps_row + gv;
-#pragma unroll 2
-            for (int rs = 0; rs < 16 / VR; ++rs) {
-              const int r = 16 * vw + rs * VR + vrow;
-              uint32_t w[VW];
-              load_words<VW>(sV + r * W + vlane * VW, w);
-              float2 f[EV / 2];
-              unpack_words<4, EXACT, VW>(w, f);
-              const float4 a4 = pp[r * Ls.ps_row];
-              const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+          const uint32_t* sV = reinterpret_cast<const uint32_t*>(vst);
+          int st0, st1;
+          tiles_of(lr0, lr1, st0, st1);
+          for (int st = st0; st < st1; ++st, ++j) {
+            const int pbuf = j & 1;
+            ok = ok && wait_warp(&p_full[pbuf], (j >> 1) & 1, abort_flag, p.err);
+            const float4 al4 = reinterpret_cast<const float4*>(alpha_s)[pbuf * 4 + q];
+            const float al[4] = {al4.x, al4.y, al4.z, al4.w};
+            if (al[0] != 1.f || al[1] != 1.f || al[2] != 1.f || al[3] != 1.f) {
 #pragma unroll
               for (int h = 0; h < NH; ++h)
 #pragma unroll
-                for (int k = 0; k < EV / 2; ++k) o[h][k] = __ffma2_rn(make_float2(av[h], av[h]), f[k], o[h][k]);
+                for (int k = 0; k < EV / 2; ++k) o[h][k] = __fmul2_rn(o[h][k], make_float2(al[h], al[h]));
             }
-          }
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&p_empty[pbuf]);
-            mbar_arrive(&vempty[vs]);
+            const int rbase = st * TILE + 16 * vw;   // this warp's 16 slot rows (rows outside the chunk: p * A_v = 0)
+            if (ok && rbase < lr1 && rbase + 16 > lr0) {
+              const float4* pp = ps + (size_t)pbuf * TILE * Ls.ps_row + gv;
+#pragma unroll 2
+              for (int rs = 0; rs < 16 / VR; ++rs) {
+                const int r = 16 * vw + rs * VR + vrow;   // tile row
+                uint32_t w[VW];
+                load_words<VW>(sV + (st * TILE + r) * W + vlane * VW, w);
+                float2 f[EV / 2];
+                unpack_words<4, EXACT, VW>(w, f);
+                const float4 a4 = pp[r * Ls.ps_row];
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int h = 0; h < NH; ++h)
+#pragma unroll
+                  for (int k = 0; k < EV / 2; ++k) o[h][k] = __ffma2_rn(make_float2(av[h], av[h]), f[k], o[h][k]);
+              }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_empty[pbuf]);
           }
           if (c1 == walk.u_end || c1 == r1) {
             if constexpr (VR > 1) {   // the lanes of one V slice took different rows: add their sums
@@ -582,7 +612,8 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
                     o[h][k] = __fadd2_rn(o[h][k], make_float2(__shfl_xor_sync(0xffffffffu, o[h][k].x, off),
                                                               __shfl_xor_sync(0xffffffffu, o[h][k].y, off)));
             }
-            named_barrier_sync(1, EV_THREADS);   // the epilogue warps are past this tile: the area is free
+            float* co = reinterpret_cast<float*>(vst);
+            named_barrier_sync(1, EV_THREADS);   // the epilogue warps are past this slot: it is free
             if (vrow == 0) {
 #pragma unroll
               for (int h = 0; h < NH; ++h)
@@ -590,9 +621,11 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
                 for (int k = 0; k < EV / 2; ++k)
                   reinterpret_cast<float2*>(co + (vw * NH + h) * D + vlane * EV)[k] = o[h][k];
             }
-            combine(walk.unit);
+            combine(co, walk.unit);
             reset();
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&vempty[vs]);
           ++i;
           if (++vs == VS) {
             vs = 0;

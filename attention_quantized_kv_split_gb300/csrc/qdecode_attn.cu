@@ -142,12 +142,12 @@ Variant pick_tc_variant(int nrep, int D, int GS) {
   v.nh = 4;
   v.hc = (nrep + 3) / 4;
   v.heads_pad = v.hc * 4;
-  v.tile = QDA_TC_TILE;
-  // K ring: three tiles (one being converted, two in flight); V ring: the rest of shared memory, 3 to 12 tiles
-  v.kstages = 3;
+  v.tile = qda_tc_slot_rows(D);   // the chunk walker's tile: one ring slot (several 128-row MMA tiles)
+  // K ring: two slots (one being converted, one in flight); V ring: what shared memory leaves, 2 to 8 slots
+  v.kstages = 2;
   const QdaTcLayout L0 = qda_tc_layout(D, 4, v.NG, v.kstages, 0);
   const long long st = ((long long)kTcSmemBudget - (long long)L0.total) / (long long)L0.vstage_bytes;
-  v.stages = (int)std::max(3LL, std::min(12LL, st));
+  v.stages = (int)std::max(2LL, std::min(8LL, st));
   v.smem = qda_tc_layout(D, 4, v.NG, v.kstages, v.stages).total;
   return v;
 }
@@ -247,7 +247,7 @@ static __device__ __align__(256) unsigned char g_qda_static_scratch[QDA_STATIC_S
 std::mutex g_static_mu;
 void* g_static_scratch_addr[kMaxDevices] = {};
 
-// The 2-D tensor map of a cache's K codes for the tensor-core kernel: rows of D / 2 bytes, boxes of 128 rows by
+// The 2-D tensor map of a cache's K codes for the tensor-core kernel: rows of D / 2 bytes, boxes of 256 rows by
 // min(D / 2, 128) bytes, 16-byte chunks swizzled within 128-byte (64-byte at D = 128) rows so that one thread per
 // row reads shared memory without bank conflicts. cuTensorMapEncodeTiled comes from the driver through the runtime.
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -270,7 +270,7 @@ cudaError_t encode_k_map(const uint32_t* k_packed, int D, long long rows, CUtens
   const cuuint64_t rb = (cuuint64_t)D / 2;
   const cuuint64_t dims[2] = {rb, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {rb};
-  const cuuint32_t box[2] = {(cuuint32_t)std::min<cuuint64_t>(rb, 128), (cuuint32_t)QDA_TC_TILE};
+  const cuuint32_t box[2] = {(cuuint32_t)std::min<cuuint64_t>(rb, 128), 256};
   const cuuint32_t elem[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t*>(k_packed), dims, strides, box,
                         elem, CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -40,3 +40,37 @@ def test_captured_call_replays_bitwise(fn_name):
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
     assert qda.qdecode_attn_device_status() == 0
+
+
+def test_replay_after_the_workspace_grew():
+    # a call captured on the library's workspace keeps working after a later eager call of a larger shape made the
+    # library grow its workspace: the outgrown buffer stays allocated, so the replay writes to valid memory
+    w = synth.small(B=2, H=8, Hkv=2, D=256, N=(700, 90), bits=4, GS=64, seed=72)
+    q, cache, N = small_case(w)
+    dev = upload_cache(*cache, w.dtype_in)
+    qd = q.cuda()
+    eager = torch.empty(qd.shape, dtype=TORCH_DT[w.dtype_out], device="cuda")
+    qda.qdecode_attn(qd, *dev, eager, N, w.Hkv, w.GS, w.bits)
+    torch.cuda.synchronize()
+    out = torch.full_like(eager, float("nan"))
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            qda.qdecode_attn(qd, *dev, out, N, w.Hkv, w.GS, w.bits, stream=s)
+    # a much larger call: far more partial slots (8192 one-row units) than any other test's shape needs
+    big = synth.small(B=512, H=64, Hkv=16, D=512, N=tuple([1] * 512), bits=4, GS=128, seed=73)
+    need_small = qda.qdecode_attn_workspace_bytes(w.B, w.H, w.Hkv, N, w.D, w.GS, w.bits)
+    need_big = qda.qdecode_attn_workspace_bytes(big.B, big.H, big.Hkv, list(big.N), big.D, big.GS, big.bits)
+    assert need_big > 2 * max(need_small, 1 << 20)
+    qb, cb, Nb = small_case(big)
+    devb = upload_cache(*cb, big.dtype_in)
+    ob = torch.empty(qb.shape, dtype=TORCH_DT[big.dtype_out], device="cuda")
+    qda.qdecode_attn(qb.cuda(), *devb, ob, Nb, big.Hkv, big.GS, big.bits)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    assert qda.qdecode_attn_device_status() == 0
