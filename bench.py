@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--workload", type=int, default=2, help="1-5: the configurations; 6: the D = 128 case")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-workload figures (workloads 3-5, multi-query, compat, GEMV, cache append, graph replay)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -75,11 +75,24 @@ def measured_peaks():
 
 
 def split_kernel_hash() -> str:
+    """A digest of every kernel and host source: recorded traffic is used only while the sources are unchanged."""
     h = hashlib.sha256()
-    for f in ("qda_split.cuh", "qda_split2.cuh", "qda_ptx.cuh", "qda_internal.h", "qdecode_attn.cu"):
-        with open(os.path.join(ROOT, "attention_quantized_kv_split_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    csrc = os.path.join(ROOT, "attention_quantized_kv_split_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
+
+
+def workload_by_index(i: int):
+    """1-5: the configurations. 6: the D = 128 case (the most common head dimension of deployed models) on the shape
+    of the 32k workload: B1 H32 Hkv8 D128 N32768, 4-bit, GS 64 -- the same 37.7 MB of cache as the 8k workload."""
+    from attention_quantized_kv_split_gb300 import synth
+    if i == 6:
+        return dataclasses.replace(synth.small(B=1, H=32, Hkv=8, D=128, N=(32768,), bits=4, GS=64, seed=20261202 + 128),
+                                   name="d128_B1_H32_Hkv8_D128_N32768_4b_GS64_bf16")
+    return synth.workload(i)
 
 
 def recorded_traffic(workload_name: str):
@@ -354,7 +367,7 @@ def run_ours(args):
     qda.lib()
     stream = torch.cuda.current_stream()
 
-    w = synth.workload(args.workload)
+    w = workload_by_index(args.workload)
     N, q, cache = make_workload(w, device)
     out = torch.empty((w.B, w.H, w.D), dtype=synth.DT[w.dtype_out], device=device)
     # The flush write evicts L2 (it is at least 2 x L2) and is long enough on the GPU (~1 GiB, ~0.16 ms) that the host
@@ -405,7 +418,6 @@ def run_ours(args):
     rsteps = min(args.steps, 300)
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(rsteps)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(rsteps)]
-    ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(rsteps)]
     for k in range(rsteps):
         flush()
         ev0[k].record(stream)
@@ -413,17 +425,18 @@ def run_ours(args):
         qda.qdecode_attn_set_split_event(ev1[k])
         call()
         qda.qdecode_attn_set_split_event(None)
-        ev2[k].record(stream)
     torch.cuda.synchronize()
     split_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev0, ev1))
-    merge_ms = statistics.mean(b.elapsed_time(c) for b, c in zip(ev1, ev2))
     peak, peak_kind = measured_peaks()
     achieved = nbytes / (split_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
-                "kernel": "qda_split2_kernel", "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                "kernel": "qda_tc_kernel" if plan["threads"] != 160 else "qda_split2_kernel", "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6800 GB/s",
-                "split_kernel_us": round(split_ms * 1e3, 3), "merge_kernel_us": round(merge_ms * 1e3, 3),
+                "split_kernel_us": round(split_ms * 1e3, 3),
+                # the rest of a call (merge kernel, its launch behind the split kernel): the whole call's time minus
+                # the split kernel's (an event recorded between the two launches would hold the merge back)
+                "call_minus_split_us": round(max(0.0, ms_per_step - split_ms) * 1e3, 3),
                 "algorithmic_bytes_per_launch": nbytes}
 
     # the size floor of this call: the same bytes read once by a plain torch reduction over one contiguous buffer, and
@@ -432,13 +445,13 @@ def run_ours(args):
     fout = torch.empty((), dtype=torch.float32, device=device)
     tiny = torch.empty(16, dtype=torch.float32, device=device)
     for _ in range(3):
-        torch.sum(fbuf, out=fout)
-    read_ms = statistics.mean(time_calls(lambda: torch.sum(fbuf, out=fout), 50, flush, stream))
+        torch.sum(fbuf, dim=0, out=fout)
+    read_ms = statistics.mean(time_calls(lambda: torch.sum(fbuf, dim=0, out=fout), 50, flush, stream))
     launch_ms = statistics.mean(time_calls(lambda: tiny.zero_(), 50, flush, stream))
     del fbuf
     stream_floor = {"read_us": round(read_ms * 1e3, 3), "read_GBps": round(nbytes / (read_ms * 1e-3) / 1e9, 1),
                     "launch_us": round(launch_ms * 1e3, 3), "bytes": nbytes,
-                    "how": "torch.sum of one contiguous fp32 buffer of the call's KV bytes, and a 16-element zero_(), "
+                    "how": "torch.sum (dim 0) of one contiguous fp32 buffer of the call's KV bytes, and a 16-element zero_(), "
                            "each after the same L2 flush, CUDA events on the launching stream, mean of 50"}
     roofline["nominal_peak"] = 7900.0
     roofline["frac_of_nominal"] = round(achieved / 7900.0, 4)
@@ -469,14 +482,11 @@ def run_ours(args):
 
     extra = {}
     if not args.no_extra:
-        # workloads 3-5, then a head dimension of 128 (the most common one in deployed models) on the shape of the
-        # 32k workload: B1 H32 Hkv8 D128 N32768, 4-bit, GS 64 (the same 37.7 MB of cache as the 8k workload)
-        d128 = dataclasses.replace(synth.small(B=1, H=32, Hkv=8, D=128, N=(32768,), bits=4, GS=64, seed=20261202 + 128),
-                                   name="d128_B1_H32_Hkv8_D128_N32768_4b_GS64_bf16")
-        for idx in (3, 4, 5, d128):
+        # workloads 3-5 and the D = 128 case
+        for idx in (3, 4, 5, 6):
             if idx == args.workload:
                 continue
-            wx = synth.workload(idx) if isinstance(idx, int) else idx
+            wx = workload_by_index(idx)
             Nx, qx, cx = make_workload(wx, device)
             ox = torch.empty((wx.B, wx.H, wx.D), dtype=synth.DT[wx.dtype_out], device=device)
             fx = qda.bind_decode_attention(qx, cx, ox, stream)
@@ -491,7 +501,8 @@ def run_ours(args):
                               "frac_of_peak": round(bx / (mx * 1e-3) / 1e9 / peak, 4), "kv_bytes": bx,
                               "split_kernel_us": round(sx * 1e3, 2),
                               "split_frac_of_peak": round(bx / (sx * 1e-3) / 1e9 / peak, 4),
-                              "split_kernel": "qda_tc_kernel" if px["threads"] != 160 else "qda_split2_kernel"}
+                              "split_kernel": "qda_tc_kernel" if px["threads"] != 160 else "qda_split2_kernel",
+                              "traffic": recorded_traffic(wx.name)}
             del cx, qx, ox
             torch.cuda.empty_cache()
         # the two-pass compat form on this workload's cache (K read in both passes)
@@ -601,7 +612,7 @@ def run_reference(args):
     import oracle as O
     from attention_quantized_kv_split_gb300 import synth
 
-    w = synth.workload(args.workload)
+    w = workload_by_index(args.workload)
     N = synth.lengths(w)
     q = synth.query(w)
     # one (sequence, KV head) unit, quantized by the oracle itself from the same generator (CPU stream)
