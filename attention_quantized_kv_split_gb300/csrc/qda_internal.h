@@ -217,13 +217,15 @@ struct QdaRowMap {
   int off_new[QDA_MAX_B + 1];
 };
 
+// pdl: launched with programmatic dependent launch behind the previous kernel on the stream, which must not write
+// anything this launch reads (the kernels of one cache append); the launch still completes after that kernel.
 cudaError_t qda_launch_quantize(const float* x, long long rows, int D, int GS, int bits, int in_dtype,
                                 uint32_t* packed, uint16_t* scales, uint16_t* biases, cudaStream_t s,
-                                const QdaRowMap* map = nullptr);
+                                const QdaRowMap* map = nullptr, bool pdl = false);
 
 // Copies every old row of a cache into its place in the appended cache (map->append = 1); W words and NG scales
-// and biases per row, for K and V.
+// and biases per row, for K and V. pdl as above.
 cudaError_t qda_launch_append_copy(const uint32_t* kp, const uint16_t* ks, const uint16_t* kb, const uint32_t* vp,
                                    const uint16_t* vs, const uint16_t* vb, uint32_t* kpo, uint16_t* kso,
                                    uint16_t* kbo, uint32_t* vpo, uint16_t* vso, uint16_t* vbo, long long rows_old,
-                                   int W, int NG, const QdaRowMap& map, cudaStream_t s);
+                                   int W, int NG, const QdaRowMap& map, cudaStream_t s, bool pdl = false);

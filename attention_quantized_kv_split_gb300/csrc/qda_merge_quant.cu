@@ -151,8 +151,15 @@ __global__ void __launch_bounds__(256) qda_quant_kernel(const float* __restrict_
   constexpr int PER = 32 / BITS;
   constexpr int W = D / PER;
   constexpr float QMAX = (float)((1 << BITS) - 1);
+  // launched behind another kernel of the same cache append (programmatic dependent launch), this one may start
+  // early: it reads nothing the other writes. It finishes only after its predecessor has (griddepcontrol.wait at
+  // the end, a no-op for an ordinary launch), so the append's last kernel completing means the whole append is done.
+  pdl_launch_dependents();
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= rows) return;
+  if (row >= rows) {
+    pdl_wait();
+    return;
+  }
   const int lane = threadIdx.x & 31;
   const float* xr = x + row * D + lane * E;
   const long long orow = mapped_row(map, row);   // the row written
@@ -221,12 +228,15 @@ __global__ void __launch_bounds__(256) qda_quant_kernel(const float* __restrict_
     sc[orow * NG + (lane * E) / GS] = (uint16_t)sbits;
     bi[orow * NG + (lane * E) / GS] = (uint16_t)bbits;
   }
+  pdl_wait();
 }
 
 // Copies the old rows of the (sequence, KV head) units into the appended cache: CTA (x, y) takes rows
 // [x * kAppendRows, (x + 1) * kAppendRows) of units y, y + gridDim.y, ... A unit's old rows are contiguous in both caches (its block
 // only moves by the new rows of the blocks before it), so the K and V codes go as flat 16-byte pieces and the
-// scales and biases as flat 16-bit values; streaming loads and stores.
+// scales and biases as flat pairs of 16-bit values (NG is even); streaming loads and stores, four 16-byte pieces of K
+// and of V in flight per thread. Launched behind the append's quantizer launches with programmatic dependent launch
+// (see qda_quant_kernel).
 constexpr int kAppendRows = 128;
 
 __global__ void __launch_bounds__(256) qda_append_copy_kernel(
@@ -248,33 +258,62 @@ __global__ void __launch_bounds__(256) qda_append_copy_kernel(
     uint4* ko4 = reinterpret_cast<uint4*>(kpo) + dst * cpr;
     uint4* vo4 = reinterpret_cast<uint4*>(vpo) + dst * cpr;
     const long long pieces = rows * cpr;
-    for (long long i = threadIdx.x; i < pieces; i += blockDim.x) {
+    const long long step = blockDim.x;
+    long long i = threadIdx.x;
+    for (; i + 3 * step < pieces; i += 4 * step) {
+      uint4 a[4], c[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        a[u] = __ldcs(k4 + i + u * step);
+        c[u] = __ldcs(v4 + i + u * step);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        __stcs(ko4 + i + u * step, a[u]);
+        __stcs(vo4 + i + u * step, c[u]);
+      }
+    }
+    for (; i < pieces; i += step) {
       const uint4 a = __ldcs(k4 + i), c = __ldcs(v4 + i);
       __stcs(ko4 + i, a);
       __stcs(vo4 + i, c);
     }
-    const long long e = rows * NG;
-    for (long long i = threadIdx.x; i < e; i += blockDim.x) {
-      kso[dst * NG + i] = ks[src * NG + i];
-      kbo[dst * NG + i] = kb[src * NG + i];
-      vso[dst * NG + i] = vs[src * NG + i];
-      vbo[dst * NG + i] = vb[src * NG + i];
+    // a row's NG 16-bit values start at a multiple of 2 * NG bytes: 32-bit pairs
+    const long long e = rows * NG / 2;
+    const uint32_t *ks2 = reinterpret_cast<const uint32_t*>(ks + src * NG), *kb2 = reinterpret_cast<const uint32_t*>(kb + src * NG);
+    const uint32_t *vs2 = reinterpret_cast<const uint32_t*>(vs + src * NG), *vb2 = reinterpret_cast<const uint32_t*>(vb + src * NG);
+    uint32_t *kso2 = reinterpret_cast<uint32_t*>(kso + dst * NG), *kbo2 = reinterpret_cast<uint32_t*>(kbo + dst * NG);
+    uint32_t *vso2 = reinterpret_cast<uint32_t*>(vso + dst * NG), *vbo2 = reinterpret_cast<uint32_t*>(vbo + dst * NG);
+    for (long long k = threadIdx.x; k < e; k += step) {
+      const uint32_t x0 = ks2[k], x1 = kb2[k], x2 = vs2[k], x3 = vb2[k];
+      kso2[k] = x0;
+      kbo2[k] = x1;
+      vso2[k] = x2;
+      vbo2[k] = x3;
     }
   }
+  pdl_wait();
 }
 
 template <int BITS, bool F16>
 cudaError_t launch_quant(const float* x, long long rows, int D, int GS, uint32_t* packed, uint16_t* sc, uint16_t* bi,
-                         cudaStream_t s, const QdaRowMap& m) {
-  const unsigned blocks = (unsigned)((rows + 7) / 8);
+                         cudaStream_t s, const QdaRowMap& m, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
   switch (D) {
-    case 64: qda_quant_kernel<BITS, 2, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi, m); break;
-    case 128: qda_quant_kernel<BITS, 4, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi, m); break;
-    case 256: qda_quant_kernel<BITS, 8, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi, m); break;
-    case 512: qda_quant_kernel<BITS, 16, F16><<<blocks, 256, 0, s>>>(x, rows, GS, packed, sc, bi, m); break;
+    case 64: return cudaLaunchKernelEx(&cfg, qda_quant_kernel<BITS, 2, F16>, x, rows, GS, packed, sc, bi, m);
+    case 128: return cudaLaunchKernelEx(&cfg, qda_quant_kernel<BITS, 4, F16>, x, rows, GS, packed, sc, bi, m);
+    case 256: return cudaLaunchKernelEx(&cfg, qda_quant_kernel<BITS, 8, F16>, x, rows, GS, packed, sc, bi, m);
+    case 512: return cudaLaunchKernelEx(&cfg, qda_quant_kernel<BITS, 16, F16>, x, rows, GS, packed, sc, bi, m);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace qda
@@ -301,27 +340,35 @@ cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool 
 
 cudaError_t qda_launch_quantize(const float* x, long long rows, int D, int GS, int bits, int in_dtype,
                                 uint32_t* packed, uint16_t* scales, uint16_t* biases, cudaStream_t s,
-                                const QdaRowMap* map) {
+                                const QdaRowMap* map, bool pdl) {
   static const QdaRowMap kIdentity = {};
   const QdaRowMap& m = map ? *map : kIdentity;
   const bool f16 = in_dtype == QDA_FP16;
   if (bits == 4) {
-    return f16 ? qda::launch_quant<4, true>(x, rows, D, GS, packed, scales, biases, s, m)
-               : qda::launch_quant<4, false>(x, rows, D, GS, packed, scales, biases, s, m);
+    return f16 ? qda::launch_quant<4, true>(x, rows, D, GS, packed, scales, biases, s, m, pdl)
+               : qda::launch_quant<4, false>(x, rows, D, GS, packed, scales, biases, s, m, pdl);
   }
-  return f16 ? qda::launch_quant<8, true>(x, rows, D, GS, packed, scales, biases, s, m)
-             : qda::launch_quant<8, false>(x, rows, D, GS, packed, scales, biases, s, m);
+  return f16 ? qda::launch_quant<8, true>(x, rows, D, GS, packed, scales, biases, s, m, pdl)
+             : qda::launch_quant<8, false>(x, rows, D, GS, packed, scales, biases, s, m, pdl);
 }
 
 cudaError_t qda_launch_append_copy(const uint32_t* kp, const uint16_t* ks, const uint16_t* kb, const uint32_t* vp,
                                    const uint16_t* vs, const uint16_t* vb, uint32_t* kpo, uint16_t* kso,
                                    uint16_t* kbo, uint32_t* vpo, uint16_t* vso, uint16_t* vbo, long long rows_old,
-                                   int W, int NG, const QdaRowMap& map, cudaStream_t s) {
+                                   int W, int NG, const QdaRowMap& map, cudaStream_t s, bool pdl) {
   if (rows_old <= 0) return cudaSuccess;
   int max_n = 0;
   for (int b = 0; b < map.B; ++b) max_n = std::max(max_n, map.n_old[b]);
-  const dim3 grid((unsigned)((max_n + qda::kAppendRows - 1) / qda::kAppendRows),
-                  (unsigned)std::min(map.B * map.Hkv, 65535));
-  qda::qda_append_copy_kernel<<<grid, 256, 0, s>>>(kp, ks, kb, vp, vs, vb, kpo, kso, kbo, vpo, vso, vbo, W, NG, map);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((max_n + qda::kAppendRows - 1) / qda::kAppendRows),
+                     (unsigned)std::min(map.B * map.Hkv, 65535));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, qda::qda_append_copy_kernel, kp, ks, kb, vp, vs, vb, kpo, kso, kbo, vpo, vso, vbo, W,
+                            NG, map);
 }

@@ -91,6 +91,23 @@ __device__ __forceinline__ void tc_issue_v(const QdaParams& p, unsigned char* vs
   }
 }
 
+// A row's NG 16-bit scale or bias values (NG * 2 bytes, aligned to that size) in one shared-memory load: value g
+// is half g & 1 of word g / 2.
+template <int NG>
+__device__ __forceinline__ void load_halves(const uint16_t* src, uint32_t (&w)[(NG + 1) / 2]) {
+  if constexpr (NG == 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else if constexpr (NG == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(src);
+    w[0] = v.x; w[1] = v.y;
+  } else {
+    static_assert(NG == 2, "2, 4 or 8 groups");
+    w[0] = *reinterpret_cast<const uint32_t*>(src);
+  }
+}
+__device__ __forceinline__ uint32_t half_of(const uint32_t* w, int g) { return (w[g >> 1] >> (16 * (g & 1))) & 0xFFFFu; }
+
 template <int D, int NH, int NG, bool EXACT>
 __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
     qda_tc_kernel(const __grid_constant__ QdaParams p, const __grid_constant__ CUtensorMap tmk) {
@@ -103,6 +120,13 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
   constexpr int A_COLS = D / 2, ACC_COLS = 16 * NG;
   constexpr int TMEM_COLS = tc_tmem_cols(2 * A_COLS + 2 * ACC_COLS);
   constexpr int KSTEPS = D / 16;
+  // the V loop two rows deep, but one with the exact codes (their extra adds would push the loop's registers over
+  // the budget); the conversion loop not unrolled (smaller code: the roles share each sub-partition's
+  // instruction cache) -- both measured faster
+  constexpr int V_UNROLL = EXACT ? 1 : 2;
+  // a row's scales and biases by one vector load per array (fewer instructions, no bank conflicts); at 8 groups the
+  // 16 live values cost spills instead
+  constexpr bool VEC_SC = NG <= 4;
   constexpr int EPI0 = QDA_TC_CONV, V0 = EPI0 + QDA_TC_EPI, PRODUCER = V0 + QDA_TC_VW, MMA_WARP = PRODUCER + 1;
   // MMA_WARP issues the MMAs of even tiles and allocates tensor memory, MMA_WARP + 1 those of odd tiles
   constexpr int EV_THREADS = (QDA_TC_EPI + QDA_TC_VW) * 32;
@@ -321,7 +345,7 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
           tc_fence_after();
           if (ok) {
             const int row = st * TILE + 32 * warp + lane;   // the slot row this thread converts
-#pragma unroll 2
+#pragma unroll 1
             for (int c = 0; c < CPR; ++c) {
               const unsigned char* src;
               if constexpr (RB == 64) {
@@ -454,10 +478,15 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
             float sc[NH];
 #pragma unroll
             for (int h = 0; h < NH; ++h) sc[h] = 0.f;
+            uint32_t ksw[NG / 2], kbw[NG / 2];
+            if constexpr (VEC_SC) {
+              load_halves<NG>(sKS + row * NG, ksw);
+              load_halves<NG>(sKB + row * NG, kbw);
+            }
 #pragma unroll
             for (int g = 0; g < NG; ++g) {
-              const float s = half_bits_to_float_rt(sKS[row * NG + g], f16);
-              const float b = half_bits_to_float_rt(sKB[row * NG + g], f16);
+              const float s = half_bits_to_float_rt(VEC_SC ? half_of(ksw, g) : sKS[row * NG + g], f16);
+              const float b = half_bits_to_float_rt(VEC_SC ? half_of(kbw, g) : sKB[row * NG + g], f16);
               const float S = p.qscale * s;
               const float Bc = p.qscale * fmaf(-OFF, s, b);
               const float4 q4 = reinterpret_cast<const float4*>(qs)[g];
@@ -499,10 +528,15 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
             // p * A_v for the V warps (buffer pbuf, free once the V warps are done with tile j - 2), sums of p * B_v
             if (j >= 2) ok = ok && wait_warp(&p_empty[pbuf], ((j >> 1) - 1) & 1, abort_flag, p.err);
             float4* psr = ps + ((size_t)pbuf * TILE + m) * Ls.ps_row;
+            uint32_t vsw[NG / 2], vbw[NG / 2];
+            if constexpr (VEC_SC) {
+              load_halves<NG>(sVS + row * NG, vsw);
+              load_halves<NG>(sVB + row * NG, vbw);
+            }
 #pragma unroll
             for (int g = 0; g < NG; ++g) {
-              const float sv = valid ? half_bits_to_float_rt(sVS[row * NG + g], f16) : 0.f;
-              const float bv = valid ? half_bits_to_float_rt(sVB[row * NG + g], f16) : 0.f;
+              const float sv = valid ? half_bits_to_float_rt(VEC_SC ? half_of(vsw, g) : sVS[row * NG + g], f16) : 0.f;
+              const float bv = valid ? half_bits_to_float_rt(VEC_SC ? half_of(vbw, g) : sVB[row * NG + g], f16) : 0.f;
               const float2 av = coeffs<4, EXACT>(sv, bv);
               psr[g] = make_float4(pr[0] * av.x, pr[1] * av.x, pr[2] * av.x, pr[3] * av.x);
 #pragma unroll
@@ -583,7 +617,7 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
             const int rbase = st * TILE + 16 * vw;   // this warp's 16 slot rows (rows outside the chunk: p * A_v = 0)
             if (ok && rbase < lr1 && rbase + 16 > lr0) {
               const float4* pp = ps + (size_t)pbuf * TILE * Ls.ps_row + gv;
-#pragma unroll 2
+#pragma unroll V_UNROLL
               for (int rs = 0; rs < 16 / VR; ++rs) {
                 const int r = 16 * vw + rs * VR + vrow;   // tile row
                 uint32_t w[VW];

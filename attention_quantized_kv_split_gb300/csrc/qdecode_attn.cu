@@ -681,19 +681,23 @@ int qdecode_cache_append(const uint32_t* k_packed, const void* k_scales, const v
   }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int W = D * bits / 32, NG = D / GS;
-  cudaError_t e = qda_launch_append_copy(
+  // the new rows' two quantizer launches first (an ordinary launch: it waits for whatever the stream did before),
+  // then the old rows' copy; the second and third launches overlap their predecessors (they read nothing those
+  // write) and each completes only after its predecessor, so the copy's completion ends the whole append
+  const long long rows_new = (long long)B * Hkv * T;
+  cudaError_t e = qda_launch_quantize(k_new, rows_new, D, GS, bits, in_dt, k_packed_out,
+                                      static_cast<uint16_t*>(k_scales_out), static_cast<uint16_t*>(k_biases_out), s,
+                                      &m, false);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = qda_launch_quantize(v_new, rows_new, D, GS, bits, in_dt, v_packed_out, static_cast<uint16_t*>(v_scales_out),
+                          static_cast<uint16_t*>(v_biases_out), s, &m, true);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = qda_launch_append_copy(
       k_packed, static_cast<const uint16_t*>(k_scales), static_cast<const uint16_t*>(k_biases), v_packed,
       static_cast<const uint16_t*>(v_scales), static_cast<const uint16_t*>(v_biases), k_packed_out,
       static_cast<uint16_t*>(k_scales_out), static_cast<uint16_t*>(k_biases_out), v_packed_out,
       static_cast<uint16_t*>(v_scales_out), static_cast<uint16_t*>(v_biases_out), (long long)Hkv * total_old, W, NG,
-      m, s);
-  if (e != cudaSuccess) return cuda_fail(e);
-  const long long rows_new = (long long)B * Hkv * T;
-  e = qda_launch_quantize(k_new, rows_new, D, GS, bits, in_dt, k_packed_out, static_cast<uint16_t*>(k_scales_out),
-                          static_cast<uint16_t*>(k_biases_out), s, &m);
-  if (e != cudaSuccess) return cuda_fail(e);
-  e = qda_launch_quantize(v_new, rows_new, D, GS, bits, in_dt, v_packed_out, static_cast<uint16_t*>(v_scales_out),
-                          static_cast<uint16_t*>(v_biases_out), s, &m);
+      m, s, true);
   if (e != cudaSuccess) return cuda_fail(e);
   return QDA_OK;
 }

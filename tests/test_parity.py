@@ -1,8 +1,8 @@
 """GPU parity: the library's decode attention against the fp64 oracle, per head, through the C ABI.
 
 Tolerance (per head): max|delta| <= 1e-2 * max|o| for bf16/fp16 outputs and <= 1e-4 * max|o| for fp32 outputs.
-Small cases compare every head; the full-size workloads compare every head of the sampled KV heads (the oracle
-quantizes those units itself from the same generated rows, and the library's quantized bytes must match its
+Small cases and the full-size workloads compare every head (for the full-size workloads the oracle quantizes each
+(sequence, KV head) unit itself from the same generated rows, and the library's quantized bytes must match its
 bytes exactly)."""
 import numpy as np
 import pytest
