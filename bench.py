@@ -235,22 +235,24 @@ def split_time(fn, steps, flush, stream):
 
 
 def cpu_oracle_task(args):
-    """One query head over one (sequence, KV head) of the cache, by the oracle as it stands: dequantize the unit's
-    packed K and V rows, then softmax(K q / sqrt(D)) V in fp64."""
+    """One (sequence, KV head) unit of the cache with all its query heads, by the oracle as it stands
+    (attention_packed: the unit's packed K and V rows dequantized once, then softmax(K q / sqrt(D)) V in fp64 per
+    query head)."""
     import oracle as O
-    spec, r0, r1, head, rows_cap = args
+    spec, b, kvh = args
     a = _shm_arrays(spec)
-    r1 = min(r1, r0 + rows_cap)
-    D, GS, bits = spec["D"], spec["GS"], spec["bits"]
-    Kd = O.dequantize(O.unpack(a["kp"][r0:r1], bits, D), a["ks"][r0:r1], a["kb"][r0:r1], GS)
-    Vd = O.dequantize(O.unpack(a["vp"][r0:r1], bits, D), a["vs"][r0:r1], a["vb"][r0:r1], GS)
-    return O.attention_head(a["q"][head], Kd, Vd)
+    H, Hkv, D = spec["H"], spec["Hkv"], spec["D"]
+    nrep = H // Hkv
+    q = a["q"].reshape(len(spec["N"]), H, D)
+    return O.attention_packed(q, a["kp"], a["ks"], a["kb"], a["vp"], a["vs"], a["vb"], spec["N"], H, Hkv, D,
+                              spec["GS"], spec["bits"], heads=[(b, kvh * nrep + j) for j in range(nrep)])
 
 
 def cpu_baseline(w, N, q, cache, pool, cores):
-    """The oracle, unchanged, on the host cores: the whole call as (sequence, KV head, query head) tasks spread over
-    one single-threaded worker process per core. The cache sits in shared memory that every worker attached before
-    the clock starts; only dequantization and attention are timed."""
+    """The oracle, unchanged, on the host cores: the whole call as (sequence, KV head) tasks -- each the oracle's
+    attention_packed over that unit's query heads -- spread over one single-threaded worker process per core. The
+    cache sits in shared memory that every worker attached before the clock starts; only dequantization and
+    attention are timed."""
     import numpy as np
     from multiprocessing import shared_memory
     arrs = {"kp": cache.kp.cpu().numpy().view(np.uint32), "ks": cache.ks.float().cpu().numpy(),
@@ -260,20 +262,16 @@ def cpu_baseline(w, N, q, cache, pool, cores):
     total = sum((a.nbytes + 63) // 64 * 64 for a in arrs.values())
     shm = shared_memory.SharedMemory(create=True, size=total)
     try:
-        spec = {"name": shm.name, "arrays": {}, "D": w.D, "GS": w.GS, "bits": w.bits}
+        spec = {"name": shm.name, "arrays": {}, "D": w.D, "GS": w.GS, "bits": w.bits, "H": w.H, "Hkv": w.Hkv,
+                "N": [int(x) for x in N]}
         off = 0
         for nm, a in arrs.items():
             np.ndarray(a.shape, dtype=a.dtype, buffer=shm.buf, offset=off)[...] = a
             spec["arrays"][nm] = (off, a.shape, a.dtype.str)
             off += (a.nbytes + 63) // 64 * 64
-        tasks = []
-        for b in range(w.B):
-            for kvh in range(w.Hkv):
-                r0, r1 = cache.unit_rows(b, kvh)
-                for j in range(w.nrep):
-                    tasks.append((spec, r0, r1, b * w.H + kvh * w.nrep + j, 1 << 62))
-        # attach and warm up every worker on a few rows of each task (not timed)
-        pool.map(cpu_oracle_task, [t[:4] + (64,) for t in tasks] * 2, chunksize=1)
+        tasks = [(spec, b, kvh) for b in range(w.B) for kvh in range(w.Hkv)]
+        # attach and warm up the workers: at least two tasks per worker (not timed)
+        pool.map(cpu_oracle_task, tasks * -(-2 * cores // len(tasks)), chunksize=1)
         # whole calls back to back for about five seconds
         rounds = 0
         t0 = time.perf_counter()
@@ -288,9 +286,10 @@ def cpu_baseline(w, N, q, cache, pool, cores):
         shm.unlink()
     nbytes = kv_bytes(w, N)
     return {"value": rounds * nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{rounds} whole calls of {w.name} back to back: {len(tasks)} (sequence, KV head, query head) "
-                      f"tasks per call, each dequantizing its KV head's rows and attending them in fp64, one "
-                      f"single-threaded worker process per core (the cache in shared memory, attached before timing)",
+            "sample": f"{rounds} whole calls of {w.name} back to back: {len(tasks)} (sequence, KV head) tasks per call, "
+                      f"each the oracle's attention_packed over that unit's {w.nrep} query heads (its rows dequantized "
+                      f"once, attention in fp64), one single-threaded worker process per core (the cache in shared "
+                      f"memory, attached before timing); {min(len(tasks), cores)} of the {cores} workers busy",
             "seconds": round(dt, 3), "ms_per_call": round(dt / rounds * 1e3, 3)}
 
 
