@@ -125,6 +125,9 @@ __host__ __device__ inline int split2_scratch_floats(int R, int NG, int NH) {
 // per 16 KB stream the cache at about 4 TB/s on GB300, per 32 KB or more at about 7 TB/s.
 #define QDA_TC_SLOT_BYTES 32768
 
+// Rows per pipeline step of the tensor-core kernel: two 128-row MMA tiles at D = 128, one at D = 256.
+__host__ __device__ inline int qda_tc_step_rows(int D) { return D == 128 ? 2 * QDA_TC_TILE : QDA_TC_TILE; }
+
 // Rows per ring slot for head dimension D (4-bit codes: D / 2 bytes per row).
 __host__ __device__ inline int qda_tc_slot_rows(int D) { return QDA_TC_SLOT_BYTES / (D / 2); }
 
@@ -135,7 +138,7 @@ struct QdaTcLayout {
   size_t b_op;         // [2] B operand: q of a unit's heads, 16 x D 16-bit values in K-major core matrices
   size_t qs;           // [2][NG][NH] fp32 sums of q per group
   size_t alpha;        // [2][4][NH] fp32 rescale factors per tile, lane quarter and head
-  size_t ps;           // [2][128][ps_row] float4: p * A_v per (row, group), four heads
+  size_t ps;           // [2][step rows][ps_row] float4: p * A_v per (row, group), four heads
   int ps_row;          // float4 per row of ps (NG, plus one against bank conflicts)
   int slot_rows;       // rows per ring slot
   size_t k_bytes;      // one K slot (slot rows x D / 2 bytes, 16-byte chunks swizzled by the tensor copy)
@@ -161,7 +164,7 @@ __host__ __device__ inline QdaTcLayout qda_tc_layout(int D, int NH, int NG, int 
   L.alpha = L.qs + 2 * (size_t)NG * NH * 4;
   L.ps = (L.alpha + 2 * 4 * (size_t)NH * 4 + 15) & ~(size_t)15;
   L.ps_row = NG + 1;
-  const size_t ps_bytes = 2 * (size_t)QDA_TC_TILE * L.ps_row * 16;
+  const size_t ps_bytes = 2 * (size_t)qda_tc_step_rows(D) * L.ps_row * 16;
   L.k_bytes = (size_t)L.slot_rows * RB;
   L.v_bytes = (size_t)L.slot_rows * RB;
   L.sc_bytes = ((size_t)L.slot_rows * NG * 2 + 15) & ~(size_t)15;

@@ -118,7 +118,10 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
   constexpr int BOXES_Y = SLOT / 256, BOXES_X = RB / BOXW;
   constexpr int EV = D >= 256 ? D / 32 : 8, VL = D / EV, VR = 32 / VL, VW = EV / 8;
   constexpr int A_COLS = D / 2, ACC_COLS = 16 * NG;
-  constexpr int TMEM_COLS = tc_tmem_cols(2 * A_COLS + 2 * ACC_COLS);
+  // rows per pipeline step: two MMA tiles at D = 128 (both tiles' A operands and accumulators, double-buffered, fit
+  // in tensor memory), so every role's per-step waits, arrivals and bookkeeping are paid once per 256 rows
+  constexpr int TPS = D == 128 ? 2 : 1, STEP = TPS * TILE;
+  constexpr int TMEM_COLS = tc_tmem_cols(2 * TPS * (A_COLS + ACC_COLS));
   constexpr int KSTEPS = D / 16;
   // the V loop two rows deep, but one with the exact codes (their extra adds would push the loop's registers over
   // the budget); the conversion loop not unrolled (smaller code: the roles share each sub-partition's
@@ -132,10 +135,11 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
   constexpr int EV_THREADS = (QDA_TC_EPI + QDA_TC_VW) * 32;
   static_assert(NH == 4, "four query heads per CTA");
   static_assert(NG >= 2 && GS >= 32 && GS % 16 == 0, "two or more groups of at least 32 codes per row");
-  static_assert(2 * A_COLS + 2 * ACC_COLS <= 512, "tensor memory");
+  static_assert(2 * TPS * (A_COLS + ACC_COLS) <= 512, "tensor memory");
   static_assert(RB == 64 || RB % 128 == 0, "K rows of 64 or 128k bytes");
   static_assert(SLOT % 256 == 0 && BOXES_X == 1, "slots of whole 256-row boxes, one box column");
-  static_assert(QDA_TC_VW * 16 == TILE && QDA_TC_CONV * 32 == TILE && QDA_TC_EPI * 32 == TILE, "warp shares");
+  static_assert(QDA_TC_VW * 16 == TILE && QDA_TC_CONV * 32 == TILE && QDA_TC_EPI * 32 == TILE && SLOT % STEP == 0,
+                "warp shares");
 
   extern __shared__ __align__(1024) unsigned char smem[];
   const int KS = p.kstages, VS = p.stages;
@@ -203,10 +207,10 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
     walk.init(p, r0, r1);
     long long c0, c1, t0;
     const bool f16 = p.f16 != 0;
-    // the 128-row tiles of a slot that a chunk [c0, c1) (slot rows lr0 .. lr1) touches: st0 .. st1 - 1
+    // the steps of a slot that a chunk [c0, c1) (slot rows lr0 .. lr1) touches: st0 .. st1 - 1
     auto tiles_of = [](int lr0, int lr1, int& st0, int& st1) {
-      st0 = lr0 / TILE;
-      st1 = (lr1 + TILE - 1) / TILE;
+      st0 = lr0 / STEP;
+      st1 = (lr1 + STEP - 1) / STEP;
     };
 
     if (warp == PRODUCER) {
@@ -248,8 +252,8 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
       const uint32_t idesc = mma_idesc_f16(TILE, 16, f16);
       // descriptor of K step 0 of B buffer 0; step s of buffer u adds (u * 32 D + 512 s) / 16 to the address field
       const uint64_t bdesc0 = smem_desc_kmajor(smem_addr(b_op), 256, 128);
-      const uint32_t a0 = tbase + ab * A_COLS;
-      const uint32_t d0 = tbase + 2 * A_COLS + ab * ACC_COLS;
+      const uint32_t a0 = tbase + ab * TPS * A_COLS;
+      const uint32_t d0 = tbase + 2 * TPS * A_COLS + ab * TPS * ACC_COLS;
       int j = 0, uidx = -1, cur_unit = -1, issued = -1;
       bool go = true;
       while (go && walk.next(p, c0, c1, t0)) {
@@ -270,9 +274,13 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
           if (lane == 0) {
             const uint64_t bd = bdesc0 + (uint64_t)((uidx & 1) * 2 * D);
 #pragma unroll
-            for (int s = 0; s < KSTEPS; ++s) {
-              // K step s covers codes of group (16 s) / GS; the group's first step starts its accumulator afresh
-              mma_f16_ts(d0 + 16 * ((16 * s) / GS), a0 + 8 * s, bd + (uint64_t)(32 * s), idesc, (16 * s) % GS != 0);
+            for (int t = 0; t < TPS; ++t) {
+#pragma unroll
+              for (int s = 0; s < KSTEPS; ++s) {
+                // K step s covers codes of group (16 s) / GS; the group's first step starts its accumulator afresh
+                mma_f16_ts(d0 + t * ACC_COLS + 16 * ((16 * s) / GS), a0 + t * A_COLS + 8 * s, bd + (uint64_t)(32 * s),
+                           idesc, (16 * s) % GS != 0);
+              }
             }
             mma_commit(&a_free[ab]);
             mma_commit(&acc_full[ab]);
@@ -343,8 +351,8 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
           // A buffer j & 1 was last read by the MMAs of tile j - 2
           if (j >= 2) ok = ok && wait_warp(&a_free[j & 1], ((j >> 1) - 1) & 1, abort_flag, p.err);
           tc_fence_after();
-          if (ok) {
-            const int row = st * TILE + 32 * warp + lane;   // the slot row this thread converts
+          for (int t = 0; t < TPS && ok; ++t) {
+            const int row = st * STEP + t * TILE + 32 * warp + lane;   // the slot row this thread converts
 #pragma unroll 1
             for (int c = 0; c < CPR; ++c) {
               const unsigned char* src;
@@ -364,10 +372,10 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
                 out[4 * t + 2] = ((wv[t] >> 8) & 0x000F000Fu) | magic;
                 out[4 * t + 3] = ((wv[t] >> 12) & 0x000F000Fu) | magic;
               }
-              tmem_st16(tl + (j & 1) * A_COLS + 16 * c, out);
+              tmem_st16(tl + ((j & 1) * TPS + t) * A_COLS + 16 * c, out);
             }
-            tmem_wait_st();
           }
+          if (ok) tmem_wait_st();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&a_full[j & 1]);
@@ -383,7 +391,8 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
     } else {
       // ---------------------------------------------------------------------------- epilogue and V warps
       const bool epi = warp < V0;
-      const int q = epi ? warp - EPI0 : (warp - V0) >> 1;   // lane quarter (rows 32 q .. 32 q + 31 of a tile)
+      // lane quarter (rows 32 q .. 32 q + 31 of a tile); a V warp's rows lie in one quarter of one tile
+      const int q = epi ? warp - EPI0 : TPS == 1 ? (warp - V0) >> 1 : (warp - V0) & 3;
       const int ev_tid = threadIdx.x - EPI0 * 32;
       // End of a segment, after both roles wrote their parts into the chunk's V slot (the combine area; its copies
       // have landed and both roles are done with it): one partial (max, sum, o[D]) per head from the four lane
@@ -458,57 +467,68 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
             const int pbuf = j & 1;
             ok = ok && wait_warp(&acc_full[pbuf], (j >> 1) & 1, abort_flag, p.err);
             tc_fence_after();
-            float acc[NG][NH];
+            float acc[TPS][NG][NH];
             if (ok) {
 #pragma unroll
-              for (int g = 0; g < NG; ++g) tmem_ld<NH>(tl + 2 * A_COLS + pbuf * ACC_COLS + 16 * g, acc[g]);
+              for (int t = 0; t < TPS; ++t)
+#pragma unroll
+                for (int g = 0; g < NG; ++g)
+                  tmem_ld<NH>(tl + 2 * TPS * A_COLS + (pbuf * TPS + t) * ACC_COLS + 16 * g, acc[t][g]);
               tmem_wait_ld();
             } else {
 #pragma unroll
-              for (int g = 0; g < NG; ++g)
+              for (int t = 0; t < TPS; ++t)
 #pragma unroll
-                for (int h = 0; h < NH; ++h) acc[g][h] = 0.f;
+                for (int g = 0; g < NG; ++g)
+#pragma unroll
+                  for (int h = 0; h < NH; ++h) acc[t][g][h] = 0.f;
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[pbuf]);
-            const int m = 32 * q + lane;     // the tile row this thread scores
-            const int row = st * TILE + m;   // its slot row
-            const bool valid = row >= lr0 && row < lr1;
-            float sc[NH];
-#pragma unroll
-            for (int h = 0; h < NH; ++h) sc[h] = 0.f;
-            uint32_t ksw[NG / 2], kbw[NG / 2];
-            if constexpr (VEC_SC) {
-              load_halves<NG>(sKS + row * NG, ksw);
-              load_halves<NG>(sKB + row * NG, kbw);
-            }
-#pragma unroll
-            for (int g = 0; g < NG; ++g) {
-              const float s = half_bits_to_float_rt(VEC_SC ? half_of(ksw, g) : sKS[row * NG + g], f16);
-              const float b = half_bits_to_float_rt(VEC_SC ? half_of(kbw, g) : sKB[row * NG + g], f16);
-              const float S = p.qscale * s;
-              const float Bc = p.qscale * fmaf(-OFF, s, b);
-              const float4 q4 = reinterpret_cast<const float4*>(qs)[g];
-              const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-              for (int h = 0; h < NH; ++h) sc[h] = fmaf(S, acc[g][h], fmaf(Bc, qv[h], sc[h]));
-            }
+            const int m = 32 * q + lane;   // the row this thread scores in each tile of the step
+            float sc[TPS][NH];
+            bool valid[TPS];
             bool need = false;
 #pragma unroll
-            for (int h = 0; h < NH; ++h) {
-              if (!valid) sc[h] = -INFINITY;
-              need |= sc[h] > m_run[h] + 8.f;
+            for (int t = 0; t < TPS; ++t) {
+              const int row = st * STEP + t * TILE + m;   // its slot row
+              valid[t] = row >= lr0 && row < lr1;
+#pragma unroll
+              for (int h = 0; h < NH; ++h) sc[t][h] = 0.f;
+              uint32_t ksw[NG / 2], kbw[NG / 2];
+              if constexpr (VEC_SC) {
+                load_halves<NG>(sKS + row * NG, ksw);
+                load_halves<NG>(sKB + row * NG, kbw);
+              }
+#pragma unroll
+              for (int g = 0; g < NG; ++g) {
+                const float s = half_bits_to_float_rt(VEC_SC ? half_of(ksw, g) : sKS[row * NG + g], f16);
+                const float b = half_bits_to_float_rt(VEC_SC ? half_of(kbw, g) : sKB[row * NG + g], f16);
+                const float S = p.qscale * s;
+                const float Bc = p.qscale * fmaf(-OFF, s, b);
+                const float4 q4 = reinterpret_cast<const float4*>(qs)[g];
+                const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                for (int h = 0; h < NH; ++h) sc[t][h] = fmaf(S, acc[t][g][h], fmaf(Bc, qv[h], sc[t][h]));
+              }
+#pragma unroll
+              for (int h = 0; h < NH; ++h) {
+                if (!valid[t]) sc[t][h] = -INFINITY;
+                need |= sc[t][h] > m_run[h] + 8.f;
+              }
             }
-            // lazy rescaling: the reference max of a head moves only when a score passes it by more than 8 (a
-            // factor 2^8 in the weights)
+            // lazy rescaling: the reference max of a head moves only when a score of the step passes it by more
+            // than 8 (a factor 2^8 in the weights)
             float alpha[NH];
 #pragma unroll
             for (int h = 0; h < NH; ++h) alpha[h] = 1.f;
             if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
               for (int h = 0; h < NH; ++h) {
-                float bm = sc[h];
+                float bm = sc[0][h];
+#pragma unroll
+                for (int t = 1; t < TPS; ++t) bm = fmaxf(bm, sc[t][h]);
 #pragma unroll
                 for (int off = 16; off >= 1; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
                 const float mn = fmaxf(m_run[h], bm);
@@ -519,28 +539,36 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
                 for (int g = 0; g < NG; ++g) pb[g][h] *= alpha[h];
               }
             }
-            float pr[NH];
+            float pr[TPS][NH];
 #pragma unroll
-            for (int h = 0; h < NH; ++h) {
-              pr[h] = valid ? ex2(sc[h] - m_run[h]) : 0.f;
-              l_run[h] += pr[h];
-            }
-            // p * A_v for the V warps (buffer pbuf, free once the V warps are done with tile j - 2), sums of p * B_v
+            for (int t = 0; t < TPS; ++t)
+#pragma unroll
+              for (int h = 0; h < NH; ++h) {
+                pr[t][h] = valid[t] ? ex2(sc[t][h] - m_run[h]) : 0.f;
+                l_run[h] += pr[t][h];
+              }
+            // p * A_v for the V warps (buffer pbuf, free once the V warps are done with step j - 2), sums of p * B_v
             if (j >= 2) ok = ok && wait_warp(&p_empty[pbuf], ((j >> 1) - 1) & 1, abort_flag, p.err);
-            float4* psr = ps + ((size_t)pbuf * TILE + m) * Ls.ps_row;
-            uint32_t vsw[NG / 2], vbw[NG / 2];
-            if constexpr (VEC_SC) {
-              load_halves<NG>(sVS + row * NG, vsw);
-              load_halves<NG>(sVB + row * NG, vbw);
-            }
 #pragma unroll
-            for (int g = 0; g < NG; ++g) {
-              const float sv = valid ? half_bits_to_float_rt(VEC_SC ? half_of(vsw, g) : sVS[row * NG + g], f16) : 0.f;
-              const float bv = valid ? half_bits_to_float_rt(VEC_SC ? half_of(vbw, g) : sVB[row * NG + g], f16) : 0.f;
-              const float2 av = coeffs<4, EXACT>(sv, bv);
-              psr[g] = make_float4(pr[0] * av.x, pr[1] * av.x, pr[2] * av.x, pr[3] * av.x);
+            for (int t = 0; t < TPS; ++t) {
+              const int row = st * STEP + t * TILE + m;
+              float4* psr = ps + ((size_t)pbuf * STEP + t * TILE + m) * Ls.ps_row;
+              uint32_t vsw[NG / 2], vbw[NG / 2];
+              if constexpr (VEC_SC) {
+                load_halves<NG>(sVS + row * NG, vsw);
+                load_halves<NG>(sVB + row * NG, vbw);
+              }
 #pragma unroll
-              for (int h = 0; h < NH; ++h) pb[g][h] = fmaf(pr[h], av.y, pb[g][h]);
+              for (int g = 0; g < NG; ++g) {
+                const float sv =
+                    valid[t] ? half_bits_to_float_rt(VEC_SC ? half_of(vsw, g) : sVS[row * NG + g], f16) : 0.f;
+                const float bv =
+                    valid[t] ? half_bits_to_float_rt(VEC_SC ? half_of(vbw, g) : sVB[row * NG + g], f16) : 0.f;
+                const float2 av = coeffs<4, EXACT>(sv, bv);
+                psr[g] = make_float4(pr[t][0] * av.x, pr[t][1] * av.x, pr[t][2] * av.x, pr[t][3] * av.x);
+#pragma unroll
+                for (int h = 0; h < NH; ++h) pb[g][h] = fmaf(pr[t][h], av.y, pb[g][h]);
+              }
             }
             if (lane == 0)
               reinterpret_cast<float4*>(alpha_s)[pbuf * 4 + q] = make_float4(alpha[0], alpha[1], alpha[2], alpha[3]);
@@ -585,7 +613,8 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
         }
       } else {
         // ------------------------------------------------------------------------------ V warps
-        const int vw = warp - V0;   // rows 16 vw .. 16 vw + 15 of every tile
+        const int vw = warp - V0;   // rows VROWS vw .. VROWS vw + VROWS - 1 of every step
+        constexpr int VROWS = 16 * TPS;
         const int vlane = lane % VL, vrow = lane / VL;
         const int gv = (vlane * EV) / GS;
         float2 o[NH][EV / 2];
@@ -614,14 +643,14 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
 #pragma unroll
                 for (int k = 0; k < EV / 2; ++k) o[h][k] = __fmul2_rn(o[h][k], make_float2(al[h], al[h]));
             }
-            const int rbase = st * TILE + 16 * vw;   // this warp's 16 slot rows (rows outside the chunk: p * A_v = 0)
-            if (ok && rbase < lr1 && rbase + 16 > lr0) {
-              const float4* pp = ps + (size_t)pbuf * TILE * Ls.ps_row + gv;
+            const int rbase = st * STEP + VROWS * vw;   // this warp's slot rows (outside the chunk: p * A_v = 0)
+            if (ok && rbase < lr1 && rbase + VROWS > lr0) {
+              const float4* pp = ps + (size_t)pbuf * STEP * Ls.ps_row + gv;
 #pragma unroll V_UNROLL
-              for (int rs = 0; rs < 16 / VR; ++rs) {
-                const int r = 16 * vw + rs * VR + vrow;   // tile row
+              for (int rs = 0; rs < VROWS / VR; ++rs) {
+                const int r = VROWS * vw + rs * VR + vrow;   // step row
                 uint32_t w[VW];
-                load_words<VW>(sV + (st * TILE + r) * W + vlane * VW, w);
+                load_words<VW>(sV + (st * STEP + r) * W + vlane * VW, w);
                 float2 f[EV / 2];
                 unpack_words<4, EXACT, VW>(w, f);
                 const float4 a4 = pp[r * Ls.ps_row];
@@ -653,7 +682,8 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
               for (int h = 0; h < NH; ++h)
 #pragma unroll
                 for (int k = 0; k < EV / 2; ++k)
-                  reinterpret_cast<float2*>(co + (vw * NH + h) * D + vlane * EV)[k] = o[h][k];
+                  reinterpret_cast<float2*>(co + ((2 * q + (TPS == 1 ? vw & 1 : vw >> 2)) * NH + h) * D + vlane * EV)[k] =
+                      o[h][k];
             }
             combine(co, walk.unit);
             reset();
