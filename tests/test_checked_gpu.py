@@ -57,6 +57,8 @@ CASES = [
     synth.small(B=2, H=8, Hkv=4, D=512, N=(5, 700), bits=4, GS=128, dtype_in="fp16", seed=63),
     synth.small(B=3, H=6, Hkv=3, D=128, N=(1, 17, 250), bits=8, GS=64, seed=64),
     synth.small(B=2, H=4, Hkv=1, D=64, N=(2, 129), bits=4, GS=32, seed=65),
+    # the tensor-core kernel at D = 128 (two MMA tiles per pipeline step, 4 groups per row)
+    synth.small(B=3, H=12, Hkv=3, D=128, N=(1, 300, 777), bits=4, GS=32, seed=66),
 ]
 
 
