@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kMergeThreads) qda_merge_kernel(const __grid_c
   const int groups = kMergeThreads / tpr;
   const int grp = tid / tpr, t = (int)blockIdx.y * tpr + (tid - grp * tpr);
 
+  pdl_launch_dependents();   // the next call's split kernel may launch now (it waits for this grid before any access)
   pdl_wait();   // the split kernel's partials are complete and visible from here on
 
   float m_run = -INFINITY, den = 0.f;

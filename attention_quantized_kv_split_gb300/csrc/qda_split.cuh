@@ -173,6 +173,23 @@ __device__ __forceinline__ void produce_range(const QdaParams& p, ChunkWalker wa
     for (int j = (i > STAGES ? i - STAGES : 0); j < i; ++j) mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1, p.err);
 }
 
+// Launches kern with programmatic dependent launch behind the previous kernel on the stream: the kernel must wait
+// (griddepcontrol.wait) before its first global-memory access.
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kern, dim3 grid, unsigned threads, size_t smem, cudaStream_t s, const Args&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Raises a kernel's dynamic shared-memory limit to the opt-in maximum, once per (kernel, device).
 template <typename K>
 cudaError_t ensure_smem_limit(K kern, size_t smem) {

@@ -214,6 +214,9 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
     fence_barrier_init();
   }
   __syncthreads();
+  // launched with programmatic dependent launch: everything above is CTA-local; the grid before this one on the
+  // stream (the previous call's merge, or whatever wrote q or the cache) is complete and visible from here on
+  pdl_wait();
   pdl_launch_dependents();
   if (r0 >= r1) return;
 
@@ -661,8 +664,7 @@ cudaError_t launch_split2(const QdaParams& p, int D, int nh, int ng, dim3 grid, 
   return with_split2_kernel<BITS, EXACT, DSET>(D, nh, ng, p.mode, [&](auto kern) -> cudaError_t {
     cudaError_t e = ensure_smem_limit(kern, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, QDA_THREADS, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, QDA_THREADS, smem, s, p);
   });
 }
 

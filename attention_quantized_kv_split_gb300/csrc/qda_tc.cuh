@@ -200,6 +200,9 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // launched with programmatic dependent launch: everything above is CTA-local; the grid before this one on the
+  // stream is complete and visible from here on
+  pdl_wait();
   pdl_launch_dependents();
 
   if (r0 < r1) {
