@@ -15,18 +15,21 @@
 //   * the A operand (the codes) goes from the registers straight into tensor memory, the B operand (q of the
 //     unit, its own 16-bit values, exact) sits in shared memory.
 // One thread issues a tcgen05 MMA about every 50 cycles whatever its N up to 128, so a tile's D / 16 MMAs take a
-// fixed time to issue; two issuing warps halve it, and every stage of a tile runs in its own warps, linked by
-// mbarriers, so that tile i + 1 is converted and multiplied while tile i's scores and tile i - 1's V rows are
-// worked on:
-//   warps 0-3   converters: K codes of a tile (lane quarter w: rows 32 w .. 32 w + 31) -> tensor memory (A), and at
-//               a new (sequence, KV head) the unit's q into the B operand and its per-group sums;
+// fixed time to issue; two issuing warps halve it, and every stage runs in its own warps, linked by mbarriers, so
+// that pipeline step i + 1 is converted and multiplied while step i's scores and step i - 1's V rows are worked on.
+// A step is one 128-row tile at D = 256 and two at D = 128 (both fit in tensor memory double-buffered; the per-step
+// waits and bookkeeping are then paid once per 256 rows):
+//   warps 0-3   converters: K codes of a step's tiles (lane quarter w: rows 32 w .. 32 w + 31 of each tile) ->
+//               tensor memory (A), and at a new (sequence, KV head) the unit's q into the B operand and its
+//               per-group sums;
 //   warps 4-7   epilogue: accumulators of their lane quarter -> scores, the online softmax (reference max per
 //               quarter and head), p * A_v per (row, group) for the V warps, sums of p and of p * B_v;
-//   warps 8-15  V: 16 rows each of every tile, all four heads, packed fp32 FMAs on the CUDA cores;
+//   warps 8-15  V: 16 rows per tile of each step (consecutive rows), all four heads, packed fp32 FMAs on the CUDA
+//               cores;
 //   warp 16     producer: 2-D tensor copies of the K tiles (their 128-byte swizzle lets one thread per row read its
 //               row without bank conflicts) into one ring, 1-D bulk copies of the V codes, scales and biases into
 //               a second;
-//   warps 17-18 issue the MMAs of even and odd tiles (double-buffered A operand and accumulators in tensor
+//   warps 17-18 issue the MMAs of even and odd steps (double-buffered A operand and accumulators in tensor
 //               memory, which warp 17 allocates and frees).
 // Every wait is bounded; after a timeout every warp still passes every barrier (with no work), so the kernel
 // always returns and frees its tensor memory.
@@ -131,7 +134,7 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
   // 16 live values cost spills instead
   constexpr bool VEC_SC = NG <= 4;
   constexpr int EPI0 = QDA_TC_CONV, V0 = EPI0 + QDA_TC_EPI, PRODUCER = V0 + QDA_TC_VW, MMA_WARP = PRODUCER + 1;
-  // MMA_WARP issues the MMAs of even tiles and allocates tensor memory, MMA_WARP + 1 those of odd tiles
+  // MMA_WARP issues the MMAs of even steps and allocates tensor memory, MMA_WARP + 1 those of odd steps
   constexpr int EV_THREADS = (QDA_TC_EPI + QDA_TC_VW) * 32;
   static_assert(NH == 4, "four query heads per CTA");
   static_assert(NG >= 2 && GS >= 32 && GS % 16 == 0, "two or more groups of at least 32 codes per row");
@@ -249,7 +252,7 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
       __syncwarp();
     } else if (warp >= MMA_WARP) {
       // ---------------------------------------------------------------------------------- MMA warps
-      // Two issuers, one per A / accumulator buffer (tile parity): one thread issues an MMA about every 50
+      // Two issuers, one per A / accumulator buffer (step parity): one thread issues an MMA about every 50
       // cycles, and two threads keep the tensor pipe twice as busy.
       const int ab = warp - MMA_WARP;
       const uint32_t idesc = mma_idesc_f16(TILE, 16, f16);
@@ -351,7 +354,7 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
         tiles_of((int)(c0 - t0), (int)(c1 - t0), st0, st1);
         const unsigned char* sK = smem + Ls.k0 + (size_t)ks * Ls.k_bytes;
         for (int st = st0; st < st1; ++st, ++j) {
-          // A buffer j & 1 was last read by the MMAs of tile j - 2
+          // A buffer j & 1 was last read by the MMAs of step j - 2
           if (j >= 2) ok = ok && wait_warp(&a_free[j & 1], ((j >> 1) - 1) & 1, abort_flag, p.err);
           tc_fence_after();
           for (int t = 0; t < TPS && ok; ++t) {

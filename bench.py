@@ -75,13 +75,16 @@ def measured_peaks():
 
 
 def split_kernel_hash() -> str:
-    """A digest of every kernel and host source: recorded traffic is used only while the sources are unchanged."""
+    """A digest of the code of every kernel and host source (comments and blank lines left out): recorded traffic
+    is used only while the code is unchanged."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_quantized_kv_split_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                code = [re.sub(r"//.*$", "", line).rstrip() for line in fh]
+            h.update(f.encode() + b"\0" + "\n".join(line for line in code if line).encode())
     return h.hexdigest()[:16]
 
 
