@@ -82,3 +82,15 @@ def test_qgemv_large_and_repeatable():
     qda.qdecode_qgemv(x.cuda(), *dev, y2, 64, 8)
     torch.cuda.synchronize()
     assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("T,bits", [(3, 8), (4, 4)])
+def test_qgemv_streamed_large_and_repeatable(T, bits):
+    # three or four input rows take the streamed form (ring of bulk-copied rows, x slices kept in registers) at an
+    # MLP size; its outputs add the K-slice sums in a fixed order, so two calls agree bit for bit
+    y1 = check(T, 14336, 4096, 64, bits, seed=12 + T)
+    x, dev, _ = make(T, 14336, 4096, 64, bits, "bf16", 12 + T)
+    y2 = torch.empty_like(y1)
+    qda.qdecode_qgemv(x.cuda(), *dev, y2, 64, bits)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
