@@ -305,7 +305,6 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
       int i = 0, j = 0, ks = 0, kph = 0, uidx = -1, cur_unit = -1;
       bool ok = true;   // false once a wait of this warp gave up: the warp then passes every barrier with no work
       while (walk.next(p, c0, c1, t0)) {
-        ok = ok && wait_warp(&kfull[ks], kph, abort_flag, p.err);
         if (walk.unit != cur_unit) {
           // a new (sequence, KV head): its q into B operand buffer (unit parity) and its sums per group, once the
           // MMAs that read that buffer (two units back) are complete -- the latest MMA of each A buffer covers
@@ -350,6 +349,9 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
           named_barrier_sync(2, QDA_TC_CONV * 32);
           if (lane == 0) mbar_arrive(&qs_full[par]);
         }
+        // the chunk's K slot, waited for after a new unit's q loads, so that these overlap its arrival (at the
+        // start of a CTA, where the first MMA then comes about 2 us sooner)
+        ok = ok && wait_warp(&kfull[ks], kph, abort_flag, p.err);
         int st0, st1;
         tiles_of((int)(c0 - t0), (int)(c1 - t0), st0, st1);
         const unsigned char* sK = smem + Ls.k0 + (size_t)ks * Ls.k_bytes;
