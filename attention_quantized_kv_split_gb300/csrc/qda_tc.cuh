@@ -130,9 +130,8 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
   // the budget); the conversion loop not unrolled (smaller code: the roles share each sub-partition's
   // instruction cache) -- both measured faster
   constexpr int V_UNROLL = EXACT ? 1 : 2;
-  // a row's scales and biases by one vector load per array (fewer instructions, no bank conflicts); at 8 groups the
-  // 16 live values cost spills instead
-  constexpr bool VEC_SC = NG <= 4;
+  // the epilogue loads its accumulators in NSPLIT runs of NGH groups (8 groups: two runs, against spills)
+  constexpr int NSPLIT = NG == 8 ? 2 : 1, NGH = NG / NSPLIT;
   constexpr int EPI0 = QDA_TC_CONV, V0 = EPI0 + QDA_TC_EPI, PRODUCER = V0 + QDA_TC_VW, MMA_WARP = PRODUCER + 1;
   // MMA_WARP issues the MMAs of even steps and allocates tensor memory, MMA_WARP + 1 those of odd steps
   constexpr int EV_THREADS = (QDA_TC_EPI + QDA_TC_VW) * 32;
@@ -475,57 +474,69 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
             const int pbuf = j & 1;
             ok = ok && wait_warp(&acc_full[pbuf], (j >> 1) & 1, abort_flag, p.err);
             tc_fence_after();
-            float acc[TPS][NG][NH];
-            if (ok) {
-#pragma unroll
-              for (int t = 0; t < TPS; ++t)
-#pragma unroll
-                for (int g = 0; g < NG; ++g)
-                  tmem_ld<NH>(tl + 2 * TPS * A_COLS + (pbuf * TPS + t) * ACC_COLS + 16 * g, acc[t][g]);
-              tmem_wait_ld();
-            } else {
-#pragma unroll
-              for (int t = 0; t < TPS; ++t)
-#pragma unroll
-                for (int g = 0; g < NG; ++g)
-#pragma unroll
-                  for (int h = 0; h < NH; ++h) acc[t][g][h] = 0.f;
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[pbuf]);
             const int m = 32 * q + lane;   // the row this thread scores in each tile of the step
             float sc[TPS][NH];
             bool valid[TPS];
-            bool need = false;
 #pragma unroll
             for (int t = 0; t < TPS; ++t) {
               const int row = st * STEP + t * TILE + m;   // its slot row
               valid[t] = row >= lr0 && row < lr1;
 #pragma unroll
               for (int h = 0; h < NH; ++h) sc[t][h] = 0.f;
-              uint32_t ksw[NG / 2], kbw[NG / 2];
-              if constexpr (VEC_SC) {
+            }
+            // the accumulators of NSPLIT runs of groups in turn (two at 8 groups: 16 live values fewer), the buffer
+            // released to the MMAs after the last run is loaded
+#pragma unroll
+            for (int hf = 0; hf < NSPLIT; ++hf) {
+              float acc[TPS][NGH][NH];
+              if (ok) {
+#pragma unroll
+                for (int t = 0; t < TPS; ++t)
+#pragma unroll
+                  for (int gg = 0; gg < NGH; ++gg)
+                    tmem_ld<NH>(tl + 2 * TPS * A_COLS + (pbuf * TPS + t) * ACC_COLS + 16 * (hf * NGH + gg), acc[t][gg]);
+                tmem_wait_ld();
+              } else {
+#pragma unroll
+                for (int t = 0; t < TPS; ++t)
+#pragma unroll
+                  for (int gg = 0; gg < NGH; ++gg)
+#pragma unroll
+                    for (int h = 0; h < NH; ++h) acc[t][gg][h] = 0.f;
+              }
+              if (hf == NSPLIT - 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[pbuf]);
+              }
+#pragma unroll
+              for (int t = 0; t < TPS; ++t) {
+                const int row = st * STEP + t * TILE + m;
+                uint32_t ksw[NG / 2], kbw[NG / 2];   // a row's scales and biases: one vector load per array
                 load_halves<NG>(sKS + row * NG, ksw);
                 load_halves<NG>(sKB + row * NG, kbw);
-              }
 #pragma unroll
-              for (int g = 0; g < NG; ++g) {
-                const float s = half_bits_to_float_rt(VEC_SC ? half_of(ksw, g) : sKS[row * NG + g], f16);
-                const float b = half_bits_to_float_rt(VEC_SC ? half_of(kbw, g) : sKB[row * NG + g], f16);
-                const float S = p.qscale * s;
-                const float Bc = p.qscale * fmaf(-OFF, s, b);
-                const float4 q4 = reinterpret_cast<const float4*>(qs)[g];
-                const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+                for (int gg = 0; gg < NGH; ++gg) {
+                  const int g = hf * NGH + gg;
+                  const float s = half_bits_to_float_rt(half_of(ksw, g), f16);
+                  const float b = half_bits_to_float_rt(half_of(kbw, g), f16);
+                  const float S = p.qscale * s;
+                  const float Bc = p.qscale * fmaf(-OFF, s, b);
+                  const float4 q4 = reinterpret_cast<const float4*>(qs)[g];
+                  const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
-                for (int h = 0; h < NH; ++h) sc[t][h] = fmaf(S, acc[t][g][h], fmaf(Bc, qv[h], sc[t][h]));
+                  for (int h = 0; h < NH; ++h) sc[t][h] = fmaf(S, acc[t][gg][h], fmaf(Bc, qv[h], sc[t][h]));
+                }
               }
+            }
+            bool need = false;
+#pragma unroll
+            for (int t = 0; t < TPS; ++t)
 #pragma unroll
               for (int h = 0; h < NH; ++h) {
                 if (!valid[t]) sc[t][h] = -INFINITY;
                 need |= sc[t][h] > m_run[h] + 8.f;
               }
-            }
             // lazy rescaling: the reference max of a head moves only when a score of the step passes it by more
             // than 8 (a factor 2^8 in the weights)
             float alpha[NH];
@@ -562,16 +573,14 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
               const int row = st * STEP + t * TILE + m;
               float4* psr = ps + ((size_t)pbuf * STEP + t * TILE + m) * Ls.ps_row;
               uint32_t vsw[NG / 2], vbw[NG / 2];
-              if constexpr (VEC_SC) {
-                load_halves<NG>(sVS + row * NG, vsw);
-                load_halves<NG>(sVB + row * NG, vbw);
-              }
+              load_halves<NG>(sVS + row * NG, vsw);
+              load_halves<NG>(sVB + row * NG, vbw);
 #pragma unroll
               for (int g = 0; g < NG; ++g) {
                 const float sv =
-                    valid[t] ? half_bits_to_float_rt(VEC_SC ? half_of(vsw, g) : sVS[row * NG + g], f16) : 0.f;
+                    valid[t] ? half_bits_to_float_rt(half_of(vsw, g), f16) : 0.f;
                 const float bv =
-                    valid[t] ? half_bits_to_float_rt(VEC_SC ? half_of(vbw, g) : sVB[row * NG + g], f16) : 0.f;
+                    valid[t] ? half_bits_to_float_rt(half_of(vbw, g), f16) : 0.f;
                 const float2 av = coeffs<4, EXACT>(sv, bv);
                 psr[g] = make_float4(pr[t][0] * av.x, pr[t][1] * av.x, pr[t][2] * av.x, pr[t][3] * av.x);
 #pragma unroll
