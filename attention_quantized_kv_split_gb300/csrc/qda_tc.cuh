@@ -111,7 +111,19 @@ __device__ __forceinline__ void load_halves(const uint16_t* src, uint32_t (&w)[(
 }
 __device__ __forceinline__ uint32_t half_of(const uint32_t* w, int g) { return (w[g >> 1] >> (16 * (g & 1))) & 0xFFFFu; }
 
-template <int D, int NH, int NG, bool EXACT>
+// Input dtype of q, scales and biases: DT = 0 bf16, 1 fp16 (compile-time: one instruction per conversion), 2 chosen
+// at run time from p.f16 (the D = 256 instances: measured faster there, the compile-time form 5-7 % slower; at
+// D = 128 it is 6 % faster).
+template <int DT>
+__device__ __forceinline__ float tc_half_to_float(uint32_t u16, bool f16) {
+  if constexpr (DT == 2) {
+    return half_bits_to_float_rt(u16, f16);
+  } else {
+    return half_bits_to_float<DT == 1>(u16);
+  }
+}
+
+template <int D, int NH, int NG, bool EXACT, int DT>
 __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
     qda_tc_kernel(const __grid_constant__ QdaParams p, const __grid_constant__ CUtensorMap tmk) {
   constexpr int TILE = QDA_TC_TILE;
@@ -211,7 +223,7 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
     ChunkWalker walk;   // chunks: a slot of SLOT rows intersected with one (sequence, KV head) and the CTA's range
     walk.init(p, r0, r1);
     long long c0, c1, t0;
-    const bool f16 = p.f16 != 0;
+    const bool f16 = DT == 2 ? p.f16 != 0 : DT == 1;
     // the steps of a slot that a chunk [c0, c1) (slot rows lr0 .. lr1) touches: st0 .. st1 - 1
     auto tiles_of = [](int lr0, int lr1, int& st0, int& st1) {
       st0 = lr0 / STEP;
@@ -335,7 +347,7 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
               const uint32_t u[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                sum += half_bits_to_float_rt(u[k] & 0xFFFFu, f16) + half_bits_to_float_rt(u[k] >> 16, f16);
+                sum += tc_half_to_float<DT>(u[k] & 0xFFFFu, f16) + tc_half_to_float<DT>(u[k] >> 16, f16);
             }
 #pragma unroll
             for (int off = 1; off < GS / 8; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
@@ -518,8 +530,8 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
 #pragma unroll
                 for (int gg = 0; gg < NGH; ++gg) {
                   const int g = hf * NGH + gg;
-                  const float s = half_bits_to_float_rt(half_of(ksw, g), f16);
-                  const float b = half_bits_to_float_rt(half_of(kbw, g), f16);
+                  const float s = tc_half_to_float<DT>(half_of(ksw, g), f16);
+                  const float b = tc_half_to_float<DT>(half_of(kbw, g), f16);
                   const float S = p.qscale * s;
                   const float Bc = p.qscale * fmaf(-OFF, s, b);
                   const float4 q4 = reinterpret_cast<const float4*>(qs)[g];
@@ -578,9 +590,9 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
 #pragma unroll
               for (int g = 0; g < NG; ++g) {
                 const float sv =
-                    valid[t] ? half_bits_to_float_rt(half_of(vsw, g), f16) : 0.f;
+                    valid[t] ? tc_half_to_float<DT>(half_of(vsw, g), f16) : 0.f;
                 const float bv =
-                    valid[t] ? half_bits_to_float_rt(half_of(vbw, g), f16) : 0.f;
+                    valid[t] ? tc_half_to_float<DT>(half_of(vbw, g), f16) : 0.f;
                 const float2 av = coeffs<4, EXACT>(sv, bv);
                 psr[g] = make_float4(pr[t][0] * av.x, pr[t][1] * av.x, pr[t][2] * av.x, pr[t][3] * av.x);
 #pragma unroll
@@ -724,10 +736,16 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
   }
 }
 
+// f16: q, scales and biases in fp16 (else bf16); the D = 128 instances take it as a template argument
 template <bool EXACT, typename Fn>
-cudaError_t with_tc_kernel(int D, int nh, int ng, Fn&& f) {
-#define QDA_TC(D_, NG_) \
-  if (D == D_ && nh == 4 && ng == NG_) return f(qda_tc_kernel<D_, 4, NG_, EXACT>);
+cudaError_t with_tc_kernel(int D, int nh, int ng, bool f16, Fn&& f) {
+#define QDA_TC(D_, NG_)                                                                          \
+  if (D == D_ && nh == 4 && ng == NG_) {                                                         \
+    if constexpr (D_ == 128)                                                                     \
+      return f16 ? f(qda_tc_kernel<D_, 4, NG_, EXACT, 1>) : f(qda_tc_kernel<D_, 4, NG_, EXACT, 0>); \
+    else                                                                                         \
+      return f(qda_tc_kernel<D_, 4, NG_, EXACT, 2>);                                             \
+  }
   QDA_TC(128, 2) QDA_TC(128, 4) QDA_TC(256, 2) QDA_TC(256, 4) QDA_TC(256, 8)
 #undef QDA_TC
   return cudaErrorInvalidValue;
