@@ -176,7 +176,7 @@ __host__ __device__ inline QdaTcLayout qda_tc_layout(int D, int NH, int NG, int 
 }
 
 // Tensor-core split kernel launches (tmap_k: the CUtensorMap of the K codes, a second kernel parameter) and their
-// occupancy, per V-code form (x1: exact codes for fp32 outputs); D in {128, 256}, nh = 4, ng = D / GS >= 2.
+// occupancy, per output form (x1: fp32 outputs); D in {128, 256}, nh = 4, ng = D / GS >= 2.
 cudaError_t qda_launch_tc_x0(const QdaParams& p, const void* tmap_k, int D, int nh, int ng, dim3 grid, size_t smem,
                              cudaStream_t s);
 cudaError_t qda_launch_tc_x1(const QdaParams& p, const void* tmap_k, int D, int nh, int ng, dim3 grid, size_t smem,

@@ -109,7 +109,9 @@ __device__ __forceinline__ void load_halves(const uint16_t* src, uint32_t (&w)[(
     w[0] = *reinterpret_cast<const uint32_t*>(src);
   }
 }
-__device__ __forceinline__ uint32_t half_of(const uint32_t* w, int g) { return (w[g >> 1] >> (16 * (g & 1))) & 0xFFFFu; }
+__device__ __forceinline__ uint32_t half_of(const uint32_t* w, int g) {
+  return (w[g >> 1] >> (16 * (g & 1))) & 0xFFFFu;
+}
 
 // Input dtype of q, scales and biases: DT = 0 bf16, 1 fp16 (compile-time: one instruction per conversion), 2 chosen
 // at run time from p.f16 (the D = 256 instances: measured faster there, the compile-time form 5-7 % slower; at
@@ -123,7 +125,40 @@ __device__ __forceinline__ float tc_half_to_float(uint32_t u16, bool f16) {
   }
 }
 
-template <int D, int NH, int NG, bool EXACT, int DT>
+// V codes as floats, per output form. 16-bit outputs: 0.5 + c / 256 (a byte permute per code). fp32 outputs:
+// 0.5 + c / 32 -- each code shifted into bits 3..6 of its byte, then a byte permute under the exponent byte 0x3F --
+// so that the code, not the offset 0.5, carries most of each value (a sum of w * (0.5 + c / 32) rounds about twice
+// as coarsely as the code part alone, against 18 times for c / 256): two shifts and masks per word plus one permute
+// per code, 3 instructions per word fewer than exact codes (2^23 + c minus 2^23).
+template <bool FP32OUT, int NW>
+__device__ __forceinline__ void tc_unpack_v(const uint32_t (&w)[NW], float2 (&f)[NW * 4]) {
+  if constexpr (FP32OUT) {
+#pragma unroll
+    for (int k = 0; k < NW; ++k) {
+      const uint32_t lo = (w[k] << 3) & 0x78787878u;   // codes 0, 2, 4, 6 at bits 3..6 of bytes 0..3
+      const uint32_t hi = (w[k] >> 1) & 0x78787878u;   // codes 1, 3, 5, 7
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t sel = 0x7054u | ((uint32_t)j << 8);   // bytes [0, 0, code << 3, 0x3F]
+        f[4 * k + j] = make_float2(__uint_as_float(__byte_perm(lo, 0x3F000000u, sel)),
+                                   __uint_as_float(__byte_perm(hi, 0x3F000000u, sel)));
+      }
+    }
+  } else {
+    unpack_words<4, false, NW>(w, f);
+  }
+}
+// s * c + b = A * f + B for the code form above: c = 32 f - 16 (fp32 outputs), c = 256 f - 128 (16-bit outputs).
+template <bool FP32OUT>
+__device__ __forceinline__ float2 tc_coeffs_v(float s, float b) {
+  if constexpr (FP32OUT) {
+    return make_float2(32.0f * s, fmaf(-16.0f, s, b));
+  } else {
+    return coeffs<4, false>(s, b);
+  }
+}
+
+template <int D, int NH, int NG, bool FP32OUT, int DT>
 __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
     qda_tc_kernel(const __grid_constant__ QdaParams p, const __grid_constant__ CUtensorMap tmk) {
   constexpr int TILE = QDA_TC_TILE;
@@ -138,10 +173,9 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
   constexpr int TPS = D == 128 ? 2 : 1, STEP = TPS * TILE;
   constexpr int TMEM_COLS = tc_tmem_cols(2 * TPS * (A_COLS + ACC_COLS));
   constexpr int KSTEPS = D / 16;
-  // the V loop two rows deep, but one with the exact codes (their extra adds would push the loop's registers over
-  // the budget); the conversion loop not unrolled (smaller code: the roles share each sub-partition's
-  // instruction cache) -- both measured faster
-  constexpr int V_UNROLL = EXACT ? 1 : 2;
+  // the V loop two rows deep for 16-bit outputs, one for fp32 outputs; the conversion loop not unrolled (smaller
+  // code: the roles share each sub-partition's instruction cache) -- each measured faster
+  constexpr int V_UNROLL = FP32OUT ? 1 : 2;
   // the epilogue loads its accumulators in NSPLIT runs of NGH groups (8 groups: two runs, against spills)
   constexpr int NSPLIT = NG == 8 ? 2 : 1, NGH = NG / NSPLIT;
   constexpr int EPI0 = QDA_TC_CONV, V0 = EPI0 + QDA_TC_EPI, PRODUCER = V0 + QDA_TC_VW, MMA_WARP = PRODUCER + 1;
@@ -593,7 +627,7 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
                     valid[t] ? tc_half_to_float<DT>(half_of(vsw, g), f16) : 0.f;
                 const float bv =
                     valid[t] ? tc_half_to_float<DT>(half_of(vbw, g), f16) : 0.f;
-                const float2 av = coeffs<4, EXACT>(sv, bv);
+                const float2 av = tc_coeffs_v<FP32OUT>(sv, bv);
                 psr[g] = make_float4(pr[t][0] * av.x, pr[t][1] * av.x, pr[t][2] * av.x, pr[t][3] * av.x);
 #pragma unroll
                 for (int h = 0; h < NH; ++h) pb[g][h] = fmaf(pr[t][h], av.y, pb[g][h]);
@@ -681,7 +715,7 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
                 uint32_t w[VW];
                 load_words<VW>(sV + (st * STEP + r) * W + vlane * VW, w);
                 float2 f[EV / 2];
-                unpack_words<4, EXACT, VW>(w, f);
+                tc_unpack_v<FP32OUT, VW>(w, f);
                 const float4 a4 = pp[r * Ls.ps_row];
                 const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
@@ -711,8 +745,8 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
               for (int h = 0; h < NH; ++h)
 #pragma unroll
                 for (int k = 0; k < EV / 2; ++k)
-                  reinterpret_cast<float2*>(co + ((2 * q + (TPS == 1 ? vw & 1 : vw >> 2)) * NH + h) * D + vlane * EV)[k] =
-                      o[h][k];
+                  reinterpret_cast<float2*>(co + ((2 * q + (TPS == 1 ? vw & 1 : vw >> 2)) * NH + h) * D +
+                                            vlane * EV)[k] = o[h][k];
             }
             combine(co, walk.unit);
             reset();
@@ -737,14 +771,14 @@ __global__ void __launch_bounds__(QDA_TC_THREADS, 1)
 }
 
 // f16: q, scales and biases in fp16 (else bf16); the D = 128 instances take it as a template argument
-template <bool EXACT, typename Fn>
+template <bool FP32OUT, typename Fn>
 cudaError_t with_tc_kernel(int D, int nh, int ng, bool f16, Fn&& f) {
 #define QDA_TC(D_, NG_)                                                                          \
   if (D == D_ && nh == 4 && ng == NG_) {                                                         \
     if constexpr (D_ == 128)                                                                     \
-      return f16 ? f(qda_tc_kernel<D_, 4, NG_, EXACT, 1>) : f(qda_tc_kernel<D_, 4, NG_, EXACT, 0>); \
+      return f16 ? f(qda_tc_kernel<D_, 4, NG_, FP32OUT, 1>) : f(qda_tc_kernel<D_, 4, NG_, FP32OUT, 0>); \
     else                                                                                         \
-      return f(qda_tc_kernel<D_, 4, NG_, EXACT, 2>);                                             \
+      return f(qda_tc_kernel<D_, 4, NG_, FP32OUT, 2>);                                           \
   }
   QDA_TC(128, 2) QDA_TC(128, 4) QDA_TC(256, 2) QDA_TC(256, 4) QDA_TC(256, 8)
 #undef QDA_TC

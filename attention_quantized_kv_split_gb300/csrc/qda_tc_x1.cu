@@ -1,4 +1,4 @@
-// Tensor-core split-kernel instantiations, exact V codes (fp32 outputs).
+// Tensor-core split-kernel instantiations, fp32 outputs (V codes as 0.5 + c / 32).
 #include "qda_tc.cuh"
 
 cudaError_t qda_launch_tc_x1(const QdaParams& p, const void* tmap_k, int D, int nh, int ng, dim3 grid, size_t smem,
