@@ -218,8 +218,10 @@ cudaError_t qda_launch_qgemv_ring(const uint16_t* x, const uint32_t* wp, const u
                                   void* y, int T, int N, int K, int GS, int bits, int f16, int out, int sms,
                                   unsigned int* err, cudaStream_t s, bool* launched);
 
-// slices: CTAs per (b, l, h), each combining D / slices values of the head dimension.
-cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool pdl, int slices, cudaStream_t s);
+// slices: CTAs per (b, l, h), each combining D / slices values of the head dimension; num_sms: the device's SMs (a
+// merge of few CTAs takes 1024 threads per CTA).
+cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool pdl, int slices, int num_sms,
+                             cudaStream_t s);
 
 // Where the quantizer writes its rows. append = 0: row i to row i. append = 1 (cache append): input row
 // i = ((b * Hkv) + kvh) * T + t goes to row Hkv * off_new[b] + kvh * (n_old[b] + T) + n_old[b] + t of the new cache,

@@ -448,7 +448,7 @@ int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, cons
   for (int b = 0; b < B; ++b) max_n = std::max(max_n, (int)N[b]);
   const long long slots = (long long)max_n * plan.num_ctas / std::max(1LL, plan.total_rows) + 2;
   const int slices = (D >= 128 && slots * D > 6LL * 2048) ? D / 64 : 1;
-  e = qda_launch_merge(p, out, out_dt, !use_event, slices, s);
+  e = qda_launch_merge(p, out, out_dt, !use_event, slices, d->num_sms, s);
   if (e != cudaSuccess) return cuda_fail(e);
   g_calls.fetch_add(1);
   return QDA_OK;
