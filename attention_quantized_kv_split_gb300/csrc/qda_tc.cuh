@@ -21,11 +21,11 @@
 // waits and bookkeeping are then paid once per 256 rows):
 //   warps 0-3   converters: K codes of a step's tiles (lane quarter w: rows 32 w .. 32 w + 31 of each tile) ->
 //               tensor memory (A), and at a new (sequence, KV head) the unit's q into the B operand and its
-//               per-group sums;
+//               per-group sums (loaded before the chunk's K slot is waited for, so the two overlap);
 //   warps 4-7   epilogue: accumulators of their lane quarter -> scores, the online softmax (reference max per
 //               quarter and head), p * A_v per (row, group) for the V warps, sums of p and of p * B_v;
 //   warps 8-15  V: 16 rows per tile of each step (consecutive rows), all four heads, packed fp32 FMAs on the CUDA
-//               cores;
+//               cores (codes as 0.5 + c / 256, or 0.5 + c / 32 for fp32 outputs);
 //   warp 16     producer: 2-D tensor copies of the K tiles (their 128-byte swizzle lets one thread per row read its
 //               row without bank conflicts) into one ring, 1-D bulk copies of the V codes, scales and biases into
 //               a second;
