@@ -170,3 +170,72 @@ def test_compat_8k_workload_sampled():
         ref = O.attention_packed_compat(qs, *unit, [N[0]], nrep, 1, w.D, w.GS, w.bits, w.dtype_in)
         compare_compat(out[:, kvh * nrep:(kvh + 1) * nrep], ref)
     assert qda.qdecode_attn_device_status() == 0
+
+
+def _clear_of_midpoints(p, dtype, margin):
+    """True when every probability p (fp64, > 0) lies farther than margin * p from the midpoint between the two
+    `dtype` values around it: any value within that relative distance of p rounds to the same `dtype` value (the
+    fp32 step the oracle takes first moves p by 2^-24 of itself, far less)."""
+    r = O.round_to(p.astype(np.float32), dtype)
+    pat = O.bits16(r, dtype).astype(np.int64)                       # positive values: patterns increase with value
+    r = r.astype(np.float64)
+    other = O.from_bits16(np.where(r > p, pat - 1, pat + 1).astype(np.uint16), dtype).astype(np.float64)
+    mid = 0.5 * (r + other)
+    return bool(np.all(np.abs(p - mid) > margin * p))
+
+
+def _exact_score_case(D, bits, GS, N, dtype, seed, margin):
+    """Two query heads whose scores are exact in `dtype`: the first group of every K row is quantized with scale
+    step (a power of two) and bias 0 (its minimum 0 and maximum (2^bits - 1) * step are planted at d = 1, 2), and
+    head j's q is sqrt(D) at d = 4 j, so its score is the row's dequantised k_{4j} = code * step -- a value with at
+    most 8 significant bits, the same on every side. Seeds are tried in turn until no probability of either head
+    lies within `margin` of a rounding midpoint of `dtype` (oracle values): then every rounding decision of the
+    compat form is the same on the GPU as in the oracle."""
+    top = 2 ** bits - 1
+    step = 2.0 ** -6 if bits == 8 else 2.0 ** -4
+    for s in range(seed, seed + 200):
+        rng = np.random.default_rng(s)
+        K = rng.uniform(0.0, top * step, (N, D)).astype(np.float32)
+        K[:, 1], K[:, 2] = 0.0, top * step
+        K[:, 0] = rng.integers(0, top + 1, N) * step
+        K[:, 4] = rng.integers(0, top + 1, N) * step
+        V = rng.standard_normal((N, D)).astype(np.float32)
+        cache = O.quantize_cache(K, V, GS, bits, dtype)
+        kp, ks, kb = cache[:3]
+        Kd = O.dequantize(O.unpack(kp, bits, D), ks, kb, GS)
+        clear = True
+        for j in range(2):
+            sc = Kd[:, 4 * j].astype(np.float64)
+            assert np.array_equal(sc, O.round_to(sc.astype(np.float32), dtype)), "scores exact in the input dtype"
+            e = np.exp(sc - sc.max())
+            clear = clear and _clear_of_midpoints(e / e.sum(), dtype, margin)
+        if clear:
+            q = torch.zeros((1, 2, D), dtype=TORCH_DT[dtype])
+            q[0, 0, 0] = q[0, 1, 4] = float(np.sqrt(D))
+            return q, cache
+    raise AssertionError("no seed without a probability near a rounding midpoint")
+
+
+@pytest.mark.parametrize("dtype_in,D,bits,GS,N,splits", [("bf16", 256, 8, 32, 64, 0), ("bf16", 256, 4, 64, 96, 3),
+                                                         ("fp16", 64, 8, 32, 24, 0), ("fp16", 256, 4, 32, 40, 2)])
+def test_compat_fp32_output_exact_where_no_rounding_is_ambiguous(dtype_in, D, bits, GS, N, splits):
+    # Where no score and no probability sits near a rounding boundary of the input dtype, the compat form has no
+    # rounding flips, so its fp32 output is held to the fp32 tolerance of the single-pass path, not the 16-bit rule.
+    # The margin 2^-15 (3.1e-5) is four times a worst-case bound on the GPU's relative error in a probability here,
+    # about 7e-6: the fp32 products of exact scores (|s| <= 4) with log2 e, the fp32 exp2, and fp32 sums of at most
+    # 96 terms for the denominator.
+    q, cache = _exact_score_case(D, bits, GS, N, dtype_in, seed=100 * D + 10 * bits + N, margin=2.0 ** -15)
+    dev = upload_cache(*cache, dtype_in)
+    out = torch.empty((1, 2, D), dtype=torch.float32, device="cuda")
+    qda.qdecode_attn_debug_force_splits(splits)
+    try:
+        qda.qdecode_attn_compat(q.cuda(), *dev, out, [N], 1, GS, bits)
+    finally:
+        qda.qdecode_attn_debug_force_splits(0)
+    torch.cuda.synchronize()
+    ref = O.attention_packed_compat(q.to(torch.float64).numpy(), *cache, [N], 2, 1, D, GS, bits, dtype_in)
+    g = out.to(torch.float64).cpu().numpy()
+    for (b, h), o in ref.items():
+        err = np.abs(g[b, h] - o).max()
+        assert err <= 1e-4 * np.abs(o).max(), f"head {h}: max|delta| {err:.3e} > {1e-4 * np.abs(o).max():.3e}"
+    assert qda.qdecode_attn_device_status() == 0
