@@ -5,13 +5,15 @@
 // not part of this workload).
 //
 // S warps own R = 4 output rows, each taking 1/S of K (S = 1, 2 or 4, chosen so that a wide matrix still spreads
-// over every SM); each step a lane takes 128 bits of codes (16 elements of 8-bit, 32 of 4-bit) per row, streamed
-// past L1, the x slice of those elements (read through the read-only path: every warp reads the same few KB of x),
+// over every SM); each step a lane takes 128 bits of codes (16 elements of 8-bit, 32 of 4-bit) per row, copied
+// past L1 into its own slots of a shared-memory ring two steps ahead (asynchronous 16-byte copies: the loads in
+// flight hold no registers), the x slice of those elements (read through the read-only path: every warp reads the same few KB of x),
 // and the row's scale and bias of that group. The dot is factored as in the attention kernels: s * sum(x * code) +
 // b * sum(x), with exact codes (a byte permute to 2^23 + code, minus 2^23) and packed f32x2 FMAs. Lanes reduce
 // by shuffles, the S parts meet in shared memory in a fixed order, and one lane writes the rounded outputs. The
 // weights are streamed once: a matrix-vector product is bound by HBM.
 #include <algorithm>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -24,6 +26,22 @@ namespace qda {
 constexpr int kGemvThreads = 256;
 constexpr int kGemvRows = 4;      // output rows per warp
 constexpr int kGemvWarps = kGemvThreads / 32;
+// depth of each lane's shared-memory ring of code loads: STAGES - 1 steps are in flight while one is worked on
+// (measured at K = 4096, N = 14336: 3 stages 8 % faster than one step ahead in registers for one input row of
+// 8-bit codes and 9 % for two rows of 4-bit codes; 4 and 6 stages no faster)
+constexpr int kGemvStages = 3;
+// dynamic shared memory of one CTA: per warp STAGES steps of R rows x 32 lanes x 16 bytes
+constexpr size_t kGemvRingBytes = (size_t)kGemvWarps * kGemvStages * kGemvRows * 32 * 16;
+
+// 16-byte asynchronous copy global -> shared (L2 only), and its group commit / wait; a thread waits for its own copies
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // elements of K per lane per step: one 128-bit load of codes
 template <int BITS>
@@ -61,16 +79,15 @@ __device__ __forceinline__ void store_out(void* y, size_t idx, float v) {
 }
 
 // resident CTAs per SM the register budget aims at: three for one input row of 8-bit codes, fewer as the x slice
-// (4-bit codes: 32 elements a step) and the accumulators grow
-template <int BITS, int T, int OUT>
+// (4-bit codes: 32 elements a step) and the accumulators grow; F16: x, scales and biases in fp16 (else bf16), a
+// template argument so that each conversion is one instruction
+template <int BITS, int T, int OUT, bool F16>
 __global__ void __launch_bounds__(kGemvThreads, T == 1 ? (BITS == 8 ? 3 : 2) : (T == 2 && BITS == 8) ? 2 : 1)
-    qda_qgemv_kernel(const uint16_t* __restrict__ x,
-                                                                const uint32_t* __restrict__ wp,
-                                                                const uint16_t* __restrict__ ws,
-                                                                const uint16_t* __restrict__ wb, void* __restrict__ y,
-                                                                int N, int K, int GS, int f16, int S) {
-  constexpr int R = kGemvRows, C = gemv_codes<BITS>();
+    qda_qgemv_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ wp, const uint16_t* __restrict__ ws,
+                     const uint16_t* __restrict__ wb, void* __restrict__ y, int N, int K, int GS, int S) {
+  constexpr int R = kGemvRows, C = gemv_codes<BITS>(), ST = kGemvStages;
   __shared__ float part[kGemvWarps][R][T];
+  extern __shared__ uint4 gemv_ring[];   // [warp][stage][row][lane]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = warp / S, sp = warp - grp * S;       // row group within the CTA's block of rows, K part
   const int kpart = K / S, kbeg = sp * kpart;
@@ -91,27 +108,32 @@ __global__ void __launch_bounds__(kGemvThreads, T == 1 ? (BITS == 8 ? 3 : 2) : (
 #pragma unroll
       for (int t = 0; t < T; ++t) bacc[r][t] = 0.f;
 
-    // the codes of the R rows are loaded one step ahead (a register double buffer), so every row's load of the next
-    // step is in flight while this step's FMAs run
-    const int kend = kbeg + kpart;
-    int k0 = kbeg + lane * C;
-    uint4 cur[R];
+    // the codes of the R rows go through a ring of ST steps in shared memory, filled by asynchronous copies ST - 1
+    // steps ahead: each lane copies its own 16 bytes per row and step and reads back only those, so its own group
+    // waits order them and no other lane is involved
     const bool live = n0 < N;
+    const int nsteps = kpart / (32 * C);
+    uint4* ring = gemv_ring + (size_t)warp * ST * R * 32 + lane;
+    auto issue = [&](int step) {
+      if (live && step < nsteps) {
+        const int ks = kbeg + step * 32 * C + lane * C;
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int n = min(n0 + r, N - 1);   // rows past N repeat the last row; their results are not written
-      cur[r] = live ? __ldcs(reinterpret_cast<const uint4*>(wp + (size_t)n * W + (size_t)k0 * BITS / 32))
-                    : make_uint4(0u, 0u, 0u, 0u);
-    }
-    for (; live && k0 < kend; k0 += 32 * C) {
-      const int kn = k0 + 32 * C;
-      uint4 nxt[R];
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int n = min(n0 + r, N - 1);
-        nxt[r] = kn < kend ? __ldcs(reinterpret_cast<const uint4*>(wp + (size_t)n * W + (size_t)kn * BITS / 32))
-                           : make_uint4(0u, 0u, 0u, 0u);
+        for (int r = 0; r < R; ++r) {
+          const int n = min(n0 + r, N - 1);   // rows past N repeat the last row; their results are not written
+          cp_async16(ring + ((step % ST) * R + r) * 32, wp + (size_t)n * W + (size_t)ks * BITS / 32);
+        }
       }
+      cp_async_commit();   // an empty group past the end keeps the count of pending groups in step
+    };
+#pragma unroll
+    for (int st = 0; st < ST - 1; ++st) issue(st);
+    for (int step = 0; live && step < nsteps; ++step) {
+      issue(step + ST - 1);   // into the slot read one step ago: its values are in registers and used
+      cp_async_wait<ST - 1>();
+      const int k0 = kbeg + step * 32 * C + lane * C;
+      uint4 cur[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) cur[r] = ring[((step % ST) * R + r) * 32];
       // the x slice of these C elements, and its sums
       float2 xv[T][C / 2];
       float xs[T];
@@ -125,8 +147,7 @@ __global__ void __launch_bounds__(kGemvThreads, T == 1 ? (BITS == 8 ? 3 : 2) : (
           const uint32_t u[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            xv[t][4 * q + i] = make_float2(half_bits_to_float_rt(u[i] & 0xFFFFu, f16 != 0),
-                                           half_bits_to_float_rt(u[i] >> 16, f16 != 0));
+            xv[t][4 * q + i] = make_float2(half_bits_to_float<F16>(u[i] & 0xFFFFu), half_bits_to_float<F16>(u[i] >> 16));
             sum += xv[t][4 * q + i].x + xv[t][4 * q + i].y;
           }
         }
@@ -136,8 +157,8 @@ __global__ void __launch_bounds__(kGemvThreads, T == 1 ? (BITS == 8 ? 3 : 2) : (
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const int n = min(n0 + r, N - 1);
-        const float s = half_bits_to_float_rt(__ldg(ws + (size_t)n * NG + g), f16 != 0);
-        const float b = half_bits_to_float_rt(__ldg(wb + (size_t)n * NG + g), f16 != 0);
+        const float s = half_bits_to_float<F16>(__ldg(ws + (size_t)n * NG + g));
+        const float b = half_bits_to_float<F16>(__ldg(wb + (size_t)n * NG + g));
         // one word of codes at a time: only its pairs are live
         constexpr int PW = 16 / BITS;   // code pairs per word
         const uint32_t wv[4] = {cur[r].x, cur[r].y, cur[r].z, cur[r].w};
@@ -158,9 +179,9 @@ __global__ void __launch_bounds__(kGemvThreads, T == 1 ? (BITS == 8 ? 3 : 2) : (
           acc[r][t] = __ffma2_rn(make_float2(s, s), d[t], acc[r][t]);
           bacc[r][t] = fmaf(b, xs[t], bacc[r][t]);
         }
-        cur[r] = nxt[r];
       }
     }
+    cp_async_wait<0>();   // nothing of this block in flight when the ring is refilled for the next
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -197,17 +218,22 @@ cudaError_t launch_qgemv_t(const uint16_t* x, const uint32_t* wp, const uint16_t
     S *= 2;
   const int rows_per_cta = (kGemvWarps / S) * kGemvRows;
   const long long blocks = (N + rows_per_cta - 1) / rows_per_cta;
-  auto kern = out == QDA_BF16 ? qda_qgemv_kernel<BITS, T, QDA_BF16>
-            : out == QDA_FP16 ? qda_qgemv_kernel<BITS, T, QDA_FP16> : qda_qgemv_kernel<BITS, T, QDA_FP32>;
-  static int occ[3] = {0, 0, 0};   // resident CTAs per SM of each output instance (same on every GB300)
-  int& o = occ[out == QDA_BF16 ? 0 : out == QDA_FP16 ? 1 : 2];
+  auto pick = [&](auto f16) {
+    constexpr bool F = decltype(f16)::value;
+    return out == QDA_BF16 ? qda_qgemv_kernel<BITS, T, QDA_BF16, F>
+         : out == QDA_FP16 ? qda_qgemv_kernel<BITS, T, QDA_FP16, F> : qda_qgemv_kernel<BITS, T, QDA_FP32, F>;
+  };
+  auto kern = f16 ? pick(std::true_type{}) : pick(std::false_type{});
+  static int occ[3][2] = {};   // resident CTAs per SM of each instance (the same on every GB300)
+  int& o = occ[out == QDA_BF16 ? 0 : out == QDA_FP16 ? 1 : 2][f16 ? 1 : 0];
   if (o == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kGemvThreads, 0);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvRingBytes);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kGemvThreads, kGemvRingBytes);
     if (e != cudaSuccess) return e;
     if (o < 1) o = 1;
   }
   const dim3 grid((unsigned)std::min<long long>(blocks, (long long)sms * o));
-  kern<<<grid, kGemvThreads, 0, s>>>(x, wp, ws, wb, y, N, K, GS, f16, S);
+  kern<<<grid, kGemvThreads, kGemvRingBytes, s>>>(x, wp, ws, wb, y, N, K, GS, S);
   return cudaGetLastError();
 }
 
