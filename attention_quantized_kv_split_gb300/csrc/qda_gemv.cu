@@ -273,13 +273,8 @@ extern "C" int qdecode_qgemv(const void* x, const uint32_t* w_packed, const void
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return qda_cuda_fail(e);
-  unsigned int* err = qda_device_error_word();
-  if (!err) return QDA_ERR_CUDA;
-  bool ring = false;
-  e = qda_launch_qgemv_ring(xs, w_packed, ws, wb, y, T, N, K, GS, bits, f16, out_dt, sms, err, s, &ring);
-  if (!ring)
-    e = bits == 8 ? qda::launch_qgemv<8>(xs, w_packed, ws, wb, y, T, N, K, GS, f16, out_dt, sms, s)
-                  : qda::launch_qgemv<4>(xs, w_packed, ws, wb, y, T, N, K, GS, f16, out_dt, sms, s);
+  e = bits == 8 ? qda::launch_qgemv<8>(xs, w_packed, ws, wb, y, T, N, K, GS, f16, out_dt, sms, s)
+                : qda::launch_qgemv<4>(xs, w_packed, ws, wb, y, T, N, K, GS, f16, out_dt, sms, s);
   if (e != cudaSuccess) return qda_cuda_fail(e);
   return QDA_OK;
 }

@@ -207,17 +207,6 @@ cudaError_t qda_occupancy_split2s_b8_x1(int D, int nh, int ng, size_t smem, int*
 // Records a CUDA runtime error for qdecode_attn_last_cuda_error() (this host thread) and returns QDA_ERR_CUDA.
 int qda_cuda_fail(cudaError_t e);
 
-// The device error word of the current device (bounded waits that give up set bits in it), or nullptr with the
-// CUDA error recorded for qdecode_attn_last_cuda_error().
-unsigned int* qda_device_error_word();
-
-// Streamed weight GEMV (qda_gemv_ring.cu): plans and launches it when the shape suits it -- T = 3 or 4 (4 for 4-bit
-// codes), K a multiple of 512 and at most 4096 -- and sets *launched; otherwise leaves *launched false and launches
-// nothing, for the direct-load kernel. Returns the launch error.
-cudaError_t qda_launch_qgemv_ring(const uint16_t* x, const uint32_t* wp, const uint16_t* ws, const uint16_t* wb,
-                                  void* y, int T, int N, int K, int GS, int bits, int f16, int out, int sms,
-                                  unsigned int* err, cudaStream_t s, bool* launched);
-
 // slices: CTAs per (b, l, h), each combining D / slices values of the head dimension; num_sms: the device's SMs (a
 // merge of few CTAs takes 1024 threads per CTA).
 cudaError_t qda_launch_merge(const QdaParams& p, void* out, int out_dtype, bool pdl, int slices, int num_sms,

@@ -458,12 +458,6 @@ int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, cons
 
 int qda_cuda_fail(cudaError_t e) { return cuda_fail(e); }
 
-unsigned int* qda_device_error_word() {
-  int dev = 0;
-  DeviceState* d = device_state(&dev);
-  return d ? d->err : nullptr;
-}
-
 extern "C" {
 
 int qdecode_attn_plan(int B, int H, int Hkv, const int32_t* N, int D, int GS, int bits, int num_sms,

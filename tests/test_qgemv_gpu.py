@@ -85,9 +85,9 @@ def test_qgemv_large_and_repeatable():
 
 
 @pytest.mark.parametrize("T,bits", [(3, 8), (4, 4)])
-def test_qgemv_streamed_large_and_repeatable(T, bits):
-    # three or four input rows take the streamed form (ring of bulk-copied rows, x slices kept in registers) at an
-    # MLP size; its outputs add the K-slice sums in a fixed order, so two calls agree bit for bit
+def test_qgemv_several_inputs_large_and_repeatable(T, bits):
+    # three or four input rows at an MLP size (the kernel's largest register use, one CTA per SM); the lanes' sums
+    # meet in a fixed order, so two calls agree bit for bit
     y1 = check(T, 14336, 4096, 64, bits, seed=12 + T)
     x, dev, _ = make(T, 14336, 4096, 64, bits, "bf16", 12 + T)
     y2 = torch.empty_like(y1)
