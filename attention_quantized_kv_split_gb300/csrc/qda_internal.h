@@ -35,6 +35,7 @@ struct QdaParams {
   int stall_chunk;            // testing aid: CTA 0's producer stops before this chunk (-1: never)
   int tile_shift;             // log2(tile_rows): pipeline tiles are powers of two
   int f16;                    // q / scales / biases are fp16 (else bf16)
+  int launch_pdl;             // host side: the lean split kernel is launched with programmatic dependent launch
   float qscale;               // log2(e) / sqrt(D): scores come out in log2 units
   int seq_off[QDA_MAX_B + 1]; // seq_off[b] = N[0] + ... + N[b-1]
 };

@@ -173,10 +173,11 @@ __device__ __forceinline__ void produce_range(const QdaParams& p, ChunkWalker wa
     for (int j = (i > STAGES ? i - STAGES : 0); j < i; ++j) mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1, p.err);
 }
 
-// Launches kern with programmatic dependent launch behind the previous kernel on the stream: the kernel must wait
-// (griddepcontrol.wait) before its first global-memory access.
+// Launches kern, with programmatic dependent launch behind the previous kernel on the stream when pdl is set (the
+// kernel waits, griddepcontrol.wait, before its first global-memory access; without the attribute that wait returns
+// at once).
 template <typename K, typename... Args>
-cudaError_t launch_pdl(K kern, dim3 grid, unsigned threads, size_t smem, cudaStream_t s, const Args&... args) {
+cudaError_t launch_pdl(K kern, dim3 grid, unsigned threads, size_t smem, cudaStream_t s, bool pdl, const Args&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(threads);
@@ -186,7 +187,7 @@ cudaError_t launch_pdl(K kern, dim3 grid, unsigned threads, size_t smem, cudaStr
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 

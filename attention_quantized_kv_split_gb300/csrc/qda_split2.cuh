@@ -664,7 +664,7 @@ cudaError_t launch_split2(const QdaParams& p, int D, int nh, int ng, dim3 grid, 
   return with_split2_kernel<BITS, EXACT, DSET>(D, nh, ng, p.mode, [&](auto kern) -> cudaError_t {
     cudaError_t e = ensure_smem_limit(kern, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, grid, QDA_THREADS, smem, s, p);
+    return launch_pdl(kern, grid, QDA_THREADS, smem, s, p.launch_pdl != 0, p);
   });
 }
 

@@ -6,7 +6,7 @@ cudaError_t qda_launch_tc_x1(const QdaParams& p, const void* tmap_k, int D, int 
   return qda::with_tc_kernel<true>(D, nh, ng, p.f16 != 0, [&](auto kern) -> cudaError_t {
     cudaError_t e = qda::ensure_smem_limit(kern, smem);
     if (e != cudaSuccess) return e;
-    return qda::launch_pdl(kern, grid, QDA_TC_THREADS, smem, s, p, *static_cast<const CUtensorMap*>(tmap_k));
+    return qda::launch_pdl(kern, grid, QDA_TC_THREADS, smem, s, true, p, *static_cast<const CUtensorMap*>(tmap_k));
   });
 }
 

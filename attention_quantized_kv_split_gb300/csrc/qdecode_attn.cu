@@ -416,6 +416,9 @@ int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const dim3 grid((unsigned)plan.num_ctas * (unsigned)v.hc);
   cudaError_t e;
+  // the lean split kernel launches behind the previous kernel with programmatic dependent launch only in the compat
+  // form's second pass (behind its first): as a call's first launch the attribute measured 0.2 us slower at 8k
+  p.launch_pdl = 0;
   if (compat) {
     p.mode = 2;   // pass A: K only, per-range statistics of the rounded scores
     p.k_only = 1;
@@ -424,6 +427,7 @@ int run_call(const void* q, const uint32_t* k_packed, const void* k_scales, cons
     p.mode = 3;   // pass B: normalised, rounded probabilities times V
     p.k_only = 0;
     p.compat = 1;
+    p.launch_pdl = 1;
   } else {
     p.mode = L > 1 ? 1 : 0;
   }
