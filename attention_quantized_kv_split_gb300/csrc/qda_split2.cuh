@@ -214,8 +214,8 @@ __global__ void __launch_bounds__(QDA_THREADS, 2) qda_split2_kernel(const __grid
     fence_barrier_init();
   }
   __syncthreads();
-  // launched with programmatic dependent launch: everything above is CTA-local; the grid before this one on the
-  // stream (the previous call's merge, or whatever wrote q or the cache) is complete and visible from here on
+  // everything above is CTA-local; when launched with programmatic dependent launch (the compat form's second pass),
+  // the grid before this one on the stream is complete and visible from here on (otherwise the wait returns at once)
   pdl_wait();
   pdl_launch_dependents();
   if (r0 >= r1) return;
